@@ -1,0 +1,544 @@
+"""Benchmark of the logsumexp hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+One step is one call of the library on one batch of the workload (default
+log_softmax over the last axis of fp32 x[4096, 393216]: rows a2 + a3 of the
+path, one kernel launch).  Prints one JSON line (rank 0).  Under torchrun each
+rank runs the whole workload on its own GPU (independent batches, weak
+scaling) with no data-path collective; the timed region is bracketed by a
+barrier and a device synchronize, and the slowest rank's time is reported.
+
+--impl reference times the CPU oracle (a plain double-precision C
+implementation) on a bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "achieved HBM GB/s and % of GB300 peak, log_softmax fp32 4096x393216"
+DEFAULT_WORKLOAD = "log_softmax_4096x393216"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------------ workloads
+
+def algorithmic_bytes(w: synth.Workload) -> int:
+    """Unique bytes one step must move: each input element read once, each output
+    element written once (fp32)."""
+    if w.op == "lse_dim0":
+        R = w.shape[0]
+        inner = w.numel // R
+        return 4 * (w.numel + inner)
+    if w.op == "log_softmax":
+        return 4 * 2 * w.numel
+    if w.op == "gn_act_lse":
+        N, C, H, W = w.shape
+        return 4 * (w.numel + 2 * C + N * H * W)
+    raise KeyError(w.op)
+
+
+# Kernels each step launches (the dominant kernel first).
+LAUNCHES = {
+    "lse_dim0": ["lse_strided_kernel"],
+    "log_softmax": ["lsm_smem_cluster_kernel"],
+    "gn_act_lse": ["gn_apply_kernel", "gn_stats_kernel"],
+}
+
+
+def make_step(L, w: synth.Workload, inputs, out, stream):
+    if w.op == "lse_dim0":
+        R = w.shape[0]
+        inner = w.numel // R
+        x = inputs["x"]
+        return lambda: L.lse_reduce(x, out, 1, R, inner, stream=stream)
+    if w.op == "log_softmax":
+        rows, cols = w.shape
+        x = inputs["x"]
+        return lambda: L.log_softmax_lastdim(x, out, rows, cols, stream=stream)
+    if w.op == "gn_act_lse":
+        N, C, H, W = w.shape
+        y, g, b = inputs["y"], inputs["gamma"], inputs["beta"]
+        G, eps = w.params["G"], w.params["eps"]
+        return lambda: L.gn_act_lse(y, g, b, out, N, C, H * W, G, eps, stream=stream)
+    raise KeyError(w.op)
+
+
+def out_shape(w: synth.Workload):
+    if w.op == "lse_dim0":
+        return w.shape[1:]
+    if w.op == "log_softmax":
+        return w.shape
+    N, C, H, W = w.shape
+    return (N, 1, H, W)
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The largest v over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v: float, world: int, device=None) -> float:
+    if world <= 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_seed_offset(rank: int) -> int:
+    """Each rank draws its own batch: seeds shifted by 1000 * rank."""
+    return 1000 * rank
+
+
+# ------------------------------------------------------------------ peaks, traffic, clocks
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "log_softmax_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, or None
+    when none was taken or the kernels changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_source_sha()
+    with open(p) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            kv = dict(item.split("=", 1) for item in line.split() if "=" in item)
+            if kv.get("kernel") == kernel and kv.get("workload") == workload:
+                if kv.get("source_sha") != sha:
+                    return None
+                return float(kv["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, every 100 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []  # (wall time, fields)
+        self.proc = None
+        self.thread = None
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            pass
+        self.target = (["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid] if uuid else
+                       ["-i", str(device_index)])
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.target, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:
+            inside = [p for (_, p) in self.samples]
+            window = "whole run (no sample fell inside the timed region)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        smax = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[4:8]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def time_oracle(w: synth.Workload, x_host, budget_s: float, max_units: int, unit_rows: int):
+    """Runs the oracle over successive slices of the sample until budget_s has
+    passed (or max_units slices are done).  Returns (bytes, seconds, units, what)."""
+    import oracle
+    t0 = time.perf_counter()
+    done_bytes = 0
+    units = 0
+    while units < max_units:
+        if w.op == "log_softmax":
+            sl = x_host[units * unit_rows:(units + 1) * unit_rows]
+            if sl.shape[0] == 0:
+                break
+            oracle.log_softmax(sl)
+            done_bytes += 8 * sl.numel()
+        elif w.op == "lse_dim0":
+            sl = x_host[:, units * unit_rows:(units + 1) * unit_rows].contiguous()
+            if sl.shape[1] == 0:
+                break
+            oracle.lse_reduce(sl, 1, sl.shape[0], sl.shape[1])
+            done_bytes += 4 * (sl.numel() + sl.shape[1])
+        else:
+            y, g, b = x_host
+            sl = y[units * unit_rows:(units + 1) * unit_rows]
+            if sl.shape[0] == 0:
+                break
+            oracle.gn_act_lse(sl, g, b, w.params["G"], w.params["eps"])
+            done_bytes += 4 * (sl.numel() + sl.shape[0] * sl.shape[2] * sl.shape[3])
+        units += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return done_bytes, time.perf_counter() - t0, units
+
+
+def oracle_sample(w: synth.Workload, inputs_dev, rows: int):
+    """The first `rows` units (rows / columns / samples) of the workload on the host."""
+    if w.op == "log_softmax":
+        return inputs_dev["x"][:rows].cpu().contiguous(), 1
+    if w.op == "lse_dim0":
+        R = w.shape[0]
+        inner = w.numel // R
+        cols = min(inner, rows * 4096)
+        return inputs_dev["x"].view(R, inner)[:, :cols].cpu().contiguous(), 4096
+    y = inputs_dev["y"][:max(1, rows // 64)].cpu().contiguous()
+    return (y, inputs_dev["gamma"].cpu(), inputs_dev["beta"].cpu()), 1
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, w: synth.Workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    shape = list(w.shape)
+    # one step = a bounded sample: 4 rows / 4096x32 columns / 1 sample
+    if w.op == "log_softmax":
+        shape[0] = min(shape[0], 4)
+        sample = f"{shape[0]} rows of {w.shape[1]}"
+    elif w.op == "lse_dim0":
+        shape[1:] = [1, min(w.numel // w.shape[0], 4096 * 32)]
+        sample = f"R={w.shape[0]} x {shape[2]} columns"
+    else:
+        shape[0] = 1
+        sample = "1 sample of the chain"
+    inputs = synth.make_inputs(w, shape=tuple(shape))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        if w.op == "log_softmax":
+            oracle.log_softmax(inputs["x"])
+            nbytes = 8 * inputs["x"].numel()
+        elif w.op == "lse_dim0":
+            x = inputs["x"].reshape(shape[0], -1)
+            oracle.lse_reduce(x, 1, x.shape[0], x.shape[1])
+            nbytes = 4 * (x.numel() + x.shape[1])
+        else:
+            oracle.gn_act_lse(inputs["y"], inputs["gamma"], inputs["beta"], w.params["G"], w.params["eps"])
+            y = inputs["y"]
+            nbytes = 4 * (y.numel() + y.shape[0] * y.shape[2] * y.shape[3])
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / len(times), 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": list(w.shape), "recipe": w.recipe,
+                   "sample_per_step": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample + " per step (single-threaded C, double precision)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w: synth.Workload):
+    world, rank, local = dist_env()
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    init_dist(world, backend)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from log_softmax_gb300 import build as libbuild
+    libbuild.build()
+    import log_softmax_gb300 as L
+    L.load_library()
+
+    # inputs resident in HBM before the timed region
+    seed_shift = rank_seed_offset(rank)
+    params = dict(w.params)
+    for k in list(params):
+        if k.endswith("seed"):
+            params[k] = params[k] + seed_shift
+    wr = synth.Workload(w.name, w.op, w.shape, w.recipe, params)
+    inputs = synth.make_inputs(wr, device=dev)
+    out = torch.empty(out_shape(w), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = make_step(L, w, inputs, out, stream)
+    nbytes = algorithmic_bytes(w)
+    in_bytes = sum(t.numel() * 4 for t in inputs.values())
+    flush = None
+    if in_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    if L.lse_device_status() != 0:
+        raise SystemExit("device status reported a bounded-wait timeout during warm-up")
+
+    sampler = ClockSampler(local).start() if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t_all0.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(1.0)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall1 = time.time()
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    status = L.lse_device_status()
+
+    per_step_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_ms = sum(per_step_ms)
+    region_ms = t_all0.elapsed_time(t_all1)
+    # With inputs larger than L2 nothing runs between steps: time the whole region.
+    # Otherwise an L2 flush runs between steps; time the steps alone.
+    local_ms = kernel_ms if flush is not None else region_ms
+    slow_ms = max_over_ranks(local_ms, world, dev)
+    total_bytes = sum_over_ranks(float(nbytes * args.steps), world, dev)
+    value = total_bytes / (slow_ms / 1e3) / 1e9
+
+    # roofline of the dominant kernel (one launch of it per step)
+    peak, peak_kind = hbm_peak()
+    launch_ms = statistics.mean(per_step_ms)
+    achieved = nbytes / (launch_ms / 1e3) / 1e9
+    dominant = LAUNCHES[w.op][0]
+    if w.op == "gn_act_lse":
+        achieved_note = ("both kernels of the step: statistics read y once, the fused pass "
+                         "reads y again; algorithmic bytes count y once")
+    else:
+        achieved_note = "one launch per step"
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dominant, w.name),
+                "kernel": dominant, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6800 GB/s",
+                "note": achieved_note}
+
+    # end to end through the public API: pinned host in -> device -> host out, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(L, w, inputs, args, dev, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        sample, unit_rows = oracle_sample(w, inputs, 256)
+        b, s, units = time_oracle(w, sample, budget_s=10.0, max_units=256, unit_rows=unit_rows)
+        what = {"log_softmax": f"{units} rows x {w.shape[1]} (first rows of the workload)",
+                "lse_dim0": f"R={w.shape[0]} x {units * 4096} columns (first columns)",
+                "gn_act_lse": f"{units} samples of [64,126,126] (first samples)"}[w.op]
+        cpu = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": what + f", {s:.1f} s single-threaded"}
+
+    if rank != 0:
+        return 0
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    line = {
+        "metric": METRIC if w.name == DEFAULT_WORKLOAD else
+        f"achieved HBM GB/s and % of GB300 peak, {w.name}",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(slow_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": list(w.shape), "recipe": w.recipe,
+                   "algorithmic_bytes_per_step": nbytes,
+                   "l2": ("inputs larger than L2 (129 MB); no flush" if flush is None else
+                          "L2 flushed (256 MB write) between steps; steps timed alone"),
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": len(LAUNCHES[w.op]) * args.steps,
+        "device_status": L.lse_status_string(status),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(L, w: synth.Workload, inputs, args, dev, world):
+    """Same metric through the public Python API with pinned host buffers: each step
+    copies its input host->device, runs the call and copies the result back."""
+    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inputs.items()}
+    for k in inputs:
+        host_in[k].copy_(inputs[k])
+    host_out = torch.empty(out_shape(w), dtype=torch.float32, pin_memory=True)
+    steps = max(1, min(args.steps, args.e2e_steps))
+
+    def one():
+        if w.op == "log_softmax":
+            L.log_softmax(host_in["x"], out=host_out)
+        elif w.op == "lse_dim0":
+            L.logsumexp(host_in["x"], dim=0, out=host_out)
+        else:
+            L.gn_act_lse_forward(host_in["y"], host_in["gamma"], host_in["beta"], w.params["G"],
+                                 w.params["eps"], out=host_out)
+
+    one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize(dev)
+    dt = time.perf_counter() - t0
+    barrier(world)
+    dt = max_over_ranks(dt, world, dev)
+    nbytes = algorithmic_bytes(w)
+    total = sum_over_ranks(float(nbytes * steps), world, dev)
+    h2d = sum(t.numel() * 4 for t in host_in.values())
+    d2h = host_out.numel() * 4
+    return {"value": round(total / dt / 1e9, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "note": "pinned host buffers; H2D copy, library call and D2H copy every step"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,135 @@
+/*
+ * lse.h — C ABI of the GB300 (sm_103a) logsumexp library, liblse.so.
+ *
+ * One operation in three forms: the numerically stable log-sum-exp
+ * reduction  lse(x) = max(x) + log(sum(exp(x - max(x))))  along one axis of an
+ * fp32 tensor.  Definitions follow three web pages on the POPCORNBENCH site:
+ *   - "FW-GLM-5-1 / l1_p29": torch.logsumexp(x, dim=0) of an (R, B, D) tensor,
+ *     task analysis (max, then log of the sum of shifted exponentials);
+ *   - "Kimi-K2.6 / l1_p24": LogSoftmax over dim 1 of a (4096, 393216) tensor,
+ *     opening analysis (x_i - max - log sum exp(x_j - max)) and its
+ *     online-softmax derivation (running max with a rescaled running sum,
+ *     merged pairwise);
+ *   - "Kimi-K2.6 / l2_p92": Conv2d -> GroupNorm -> Tanh -> HardSwish ->
+ *     residual add -> LogSumExp over channels; the GroupNorm discussion
+ *     (per-sample, per-group mean and population variance over C/G channels
+ *     and H*W, (x - mean)/sqrt(var + eps), per-channel affine weight and bias)
+ *     and the HardSwish definition t * min(max(t + 3, 0), 6) / 6.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers to caller-owned memory, fp32,
+ *     contiguous (row-major, last index fastest).  The library never frees or
+ *     keeps them.  Inputs and outputs must not overlap.
+ *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
+ *     stream).  A return of LSE_OK means the launch was enqueued; kernel-time
+ *     faults surface on the next synchronising CUDA call, as usual.
+ *   - Argument errors are detected on the host before any launch and return a
+ *     status; nothing is enqueued then.  The library never aborts or traps.
+ *   - A call whose output has no elements returns LSE_OK and launches nothing.
+ *   - Pointers need 4-byte alignment.  16-byte alignment (and a row length that
+ *     keeps rows 16-byte aligned) selects the vectorised / bulk-copy kernels;
+ *     otherwise a scalar kernel runs with the same results.
+ *   - Special values: a NaN in the reduced set gives NaN; else a +inf gives
+ *     +inf; else a set that is all -inf gives -inf; -inf entries among finite
+ *     ones contribute nothing.  log_softmax is x - lse in IEEE arithmetic, so
+ *     a row holding +inf gives NaN at the +inf and -inf elsewhere, and an
+ *     all -inf row gives NaN throughout.
+ *   - Accuracy: fp32 storage and accumulation; results agree with a double
+ *     precision evaluation within |err| <= 2e-5 + 1e-6 * |ref|.
+ */
+#ifndef LSE_H
+#define LSE_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LSE_OK = 0,
+    LSE_ERR_NULL = 1,        /* a required pointer is NULL                                  */
+    LSE_ERR_SIZE = 2,        /* a size is negative, zero where it must not be, inconsistent, */
+                             /* or too large (element counts must fit in int64)             */
+    LSE_ERR_ALIGN = 3,       /* a pointer is not 4-byte aligned                             */
+    LSE_ERR_CUDA = 4,        /* a CUDA call failed; lse_last_cuda_error() has the code      */
+    LSE_ERR_UNSUPPORTED = 5, /* the device cannot run the kernel (not sm_103a, no clusters) */
+    LSE_ERR_VALUE = 6,       /* a scalar argument is out of range (e.g. eps < 0 or NaN)     */
+    LSE_ERR_TIMEOUT = 7      /* a kernel gave up waiting on a bulk copy (device status)     */
+} lse_status_t;
+
+/*
+ * lse_reduce — logsumexp over the middle axis of a contiguous (outer, R, inner)
+ * tensor:   out[o, i] = lse over r of x[o, r, i].
+ * The reduced axis has stride `inner` elements; logsumexp(x, dim=d) of any
+ * contiguous tensor is this call with outer = prod(shape[:d]), R = shape[d],
+ * inner = prod(shape[d+1:]).  The dim-0 form of "FW-GLM-5-1 / l1_p29" is
+ * outer = 1, R, inner = B*D.
+ *   x     [outer * R * inner] fp32, device, read only.
+ *   out   [outer * inner]     fp32, device, written.
+ *   outer >= 0, inner >= 0; R >= 1 when outer * inner > 0 (R = 0 would be the
+ *   empty-set value -inf, which this call rejects with LSE_ERR_SIZE).
+ */
+lse_status_t lse_reduce(const float* x, float* out, int64_t outer, int64_t R, int64_t inner,
+                        cudaStream_t stream);
+
+/*
+ * log_softmax_lastdim — row-wise log_softmax of a contiguous (rows, cols) tensor
+ * ("Kimi-K2.6 / l1_p24"):   out[r, j] = x[r, j] - lse over k of x[r, k].
+ *   x    [rows * cols] fp32, device, read only.
+ *   out  [rows * cols] fp32, device, written (must not alias x).
+ *   rows >= 0, cols >= 0.
+ * Rows up to a few MB are staged on chip (registers, or shared memory of a
+ * thread-block cluster) so that x is read from HBM once.
+ */
+lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64_t cols,
+                                 cudaStream_t stream);
+
+/*
+ * gn_act_lse — GroupNorm -> tanh -> hardswish -> residual add -> logsumexp over
+ * channels, keepdim ("Kimi-K2.6 / l2_p92", the chain after its Conv2d):
+ *   mean[n,g], var[n,g] : population statistics of the C/G channels of group g
+ *                         of sample n over all HW positions;
+ *   z   = (y[n,c,p] - mean[n,g]) / sqrt(var[n,g] + eps) * gamma[c] + beta[c]
+ *   r   = y[n,c,p] + hardswish(tanh(z)),  hardswish(t) = t*min(max(t+3,0),6)/6
+ *   out[n,p] = lse over c of r          (out is [N, 1, H, W] with HW = H*W)
+ *   y      [N * C * HW] fp32 NCHW, device, read only.
+ *   gamma  [C], beta [C] fp32, device, read only.
+ *   out    [N * HW] fp32, device, written.
+ *   N >= 0, HW >= 0, C >= 1, G >= 1, C % G == 0; eps >= 0 and finite.
+ * The per-(n, g) statistics need 2*N*G floats of scratch.  The library takes
+ * them, stream-ordered, from a memory pool it owns on the current device
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`), so concurrent calls on
+ * different streams never share scratch.  lse_release_workspace() returns the
+ * pool's idle memory to the device.
+ */
+lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, float* out,
+                        int64_t N, int64_t C, int64_t HW, int64_t G, float eps,
+                        cudaStream_t stream);
+
+/* Returns the idle memory of the library's scratch pools to the device. */
+lse_status_t lse_release_workspace(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device-side
+ * status on the current device: LSE_OK, or LSE_ERR_TIMEOUT when a kernel gave
+ * up waiting on a bulk copy (its outputs are then unspecified).  Bounded waits
+ * end after about one second; nothing in the library waits without a limit.
+ */
+lse_status_t lse_device_status(cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* lse_status_string(lse_status_t status);
+
+/* The cudaError_t of the most recent LSE_ERR_CUDA on the calling thread (0 if none). */
+int lse_last_cuda_error(void);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+int lse_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSE_H */

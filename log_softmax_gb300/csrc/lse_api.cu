@@ -1,0 +1,223 @@
+// C ABI of liblse.so: argument checks, variant choice, scratch, status.
+// Declarations and the contract of each entry point are in include/lse.h.
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/lse.h"
+#include "launch.h"
+
+namespace lse {
+
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    DeviceInfo info;
+    cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+thread_local int g_last_cuda_error = 0;
+
+lse_status_t cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return LSE_ERR_CUDA;
+}
+
+// Per-device facts, queried once with that device current.
+lse_status_t device_state(DeviceState** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return LSE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        DeviceInfo d;
+        d.device = dev;
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+                cudaSuccess)
+            return cuda_fail(e);
+        // The kernels are built for sm_103a only.
+        if (d.cc_major != 10 || d.cc_minor != 3) return LSE_ERR_UNSUPPORTED;
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e);
+        d.status = static_cast<int*>(p);
+        s.info = d;
+        s.ready = true;
+    }
+    *out = &s;
+    return LSE_OK;
+}
+
+// The library's own stream-ordered pool on this device (idle memory is kept
+// until lse_release_workspace()).
+lse_status_t device_pool(DeviceState* s, cudaMemPool_t* pool) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!s->pool) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = s->info.device;
+        cudaError_t e = cudaMemPoolCreate(&s->pool, &props);
+        if (e != cudaSuccess) {
+            s->pool = nullptr;
+            return cuda_fail(e);
+        }
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(s->pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    *pool = s->pool;
+    return LSE_OK;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+}  // namespace lse
+
+using namespace lse;
+
+extern "C" {
+
+lse_status_t lse_reduce(const float* x, float* out, int64_t outer, int64_t R, int64_t inner,
+                        cudaStream_t stream) {
+    if (outer < 0 || R < 0 || inner < 0) return LSE_ERR_SIZE;
+    int64_t nout = 0, nin = 0;
+    if (!mul_ok(outer, inner, &nout) || !mul_ok(nout, R, &nin) || nin > INT64_MAX / 4)
+        return LSE_ERR_SIZE;
+    if (nout == 0) return LSE_OK;
+    if (R == 0) return LSE_ERR_SIZE;
+    if (!x || !out) return LSE_ERR_NULL;
+    if (!aligned4(x) || !aligned4(out)) return LSE_ERR_ALIGN;
+    DeviceState* s = nullptr;
+    lse_status_t st = device_state(&s);
+    if (st != LSE_OK) return st;
+    cudaError_t e;
+    if (inner == 1) {
+        // Contiguous reduced axis: the row statistic of form 2, one value per row.
+        if (R <= kRegRowMaxCols)
+            e = launch_rows_reg(s->info, x, out, outer, R, 1, stream);
+        else
+            e = launch_rows_stream(s->info, x, out, outer, R, 1, stream);
+    } else {
+        e = launch_lse_strided(s->info, x, out, outer, R, inner, stream);
+    }
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+}
+
+lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64_t cols,
+                                 cudaStream_t stream) {
+    if (rows < 0 || cols < 0) return LSE_ERR_SIZE;
+    int64_t n = 0;
+    if (!mul_ok(rows, cols, &n) || n > INT64_MAX / 4) return LSE_ERR_SIZE;
+    if (n == 0) return LSE_OK;
+    if (!x || !out) return LSE_ERR_NULL;
+    if (!aligned4(x) || !aligned4(out)) return LSE_ERR_ALIGN;
+    DeviceState* s = nullptr;
+    lse_status_t st = device_state(&s);
+    if (st != LSE_OK) return st;
+    cudaError_t e;
+    const int force = env_int("LSE_LSM_VARIANT", 0);  // 1 registers, 2 cluster smem, 3 streaming
+    if ((force == 0 && cols <= kRegRowMaxCols) || (force == 1 && cols <= kRegRowMaxCols)) {
+        e = launch_rows_reg(s->info, x, out, rows, cols, 0, stream);
+    } else {
+        e = cudaErrorNotSupported;
+        if (force == 0 || force == 2) e = launch_lsm_smem_cluster(s->info, x, out, rows, cols, stream);
+        if (e == cudaErrorNotSupported) {
+            (void)cudaGetLastError();
+            e = launch_rows_stream(s->info, x, out, rows, cols, 0, stream);
+        }
+    }
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+}
+
+lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, float* out,
+                        int64_t N, int64_t C, int64_t HW, int64_t G, float eps,
+                        cudaStream_t stream) {
+    if (N < 0 || HW < 0 || C <= 0 || G <= 0 || C % G != 0) return LSE_ERR_SIZE;
+    if (C > kGnMaxChannels) return LSE_ERR_SIZE;
+    int64_t nchw = 0, nhw = 0, ng = 0;
+    if (!mul_ok(N, C, &nchw) || !mul_ok(nchw, HW, &nchw) || nchw > INT64_MAX / 4 ||
+        !mul_ok(N, HW, &nhw) || !mul_ok(N, G, &ng))
+        return LSE_ERR_SIZE;
+    if (!(eps >= 0.f) || eps == __builtin_inff()) return LSE_ERR_VALUE;
+    if (nhw == 0) return LSE_OK;
+    if (!y || !gamma || !beta || !out) return LSE_ERR_NULL;
+    if (!aligned4(y) || !aligned4(gamma) || !aligned4(beta) || !aligned4(out)) return LSE_ERR_ALIGN;
+    DeviceState* s = nullptr;
+    lse_status_t st = device_state(&s);
+    if (st != LSE_OK) return st;
+    cudaMemPool_t pool = nullptr;
+    if ((st = device_pool(s, &pool)) != LSE_OK) return st;
+    void* stats = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&stats, (size_t)ng * 2 * sizeof(float), pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_gn_act_lse(s->info, y, gamma, beta, out, N, C, HW, G, eps, static_cast<float*>(stats),
+                          stream);
+    cudaError_t ef = cudaFreeAsync(stats, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (ef != cudaSuccess) return cuda_fail(ef);
+    return LSE_OK;
+}
+
+lse_status_t lse_release_workspace(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_dev[d].pool) {
+            cudaError_t e = cudaMemPoolTrimTo(g_dev[d].pool, 0);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+    }
+    return LSE_OK;
+}
+
+lse_status_t lse_device_status(cudaStream_t stream) {
+    DeviceState* s = nullptr;
+    lse_status_t st = device_state(&s);
+    if (st != LSE_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int v = 0;
+    e = cudaMemcpy(&v, s->info.status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(s->info.status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return LSE_ERR_TIMEOUT;
+    }
+    return LSE_OK;
+}
+
+const char* lse_status_string(lse_status_t status) {
+    switch (status) {
+        case LSE_OK: return "ok";
+        case LSE_ERR_NULL: return "null pointer argument";
+        case LSE_ERR_SIZE: return "invalid size argument";
+        case LSE_ERR_ALIGN: return "pointer not 4-byte aligned";
+        case LSE_ERR_CUDA: return "CUDA error (see lse_last_cuda_error)";
+        case LSE_ERR_UNSUPPORTED: return "device not supported (needs sm_103a)";
+        case LSE_ERR_VALUE: return "invalid scalar argument";
+        case LSE_ERR_TIMEOUT: return "a kernel timed out waiting on a bulk copy";
+    }
+    return "unknown status";
+}
+
+int lse_last_cuda_error(void) { return g_last_cuda_error; }
+
+int lse_version(void) { return 100; }
+
+}  // extern "C"

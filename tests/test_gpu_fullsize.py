@@ -1,0 +1,99 @@
+"""The five workloads at full size, in the launch configuration the bench times
+(GPU only).  Outputs the oracle can afford are checked element by element on a
+seeded sample; every output is checked against properties that hold at any size.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from log_softmax_gb300 import build
+    build.build()
+    import log_softmax_gb300 as L
+    L.load_library()
+    torch.cuda.set_device(0)
+    yield L
+    assert L.lse_device_status() == 0
+    torch.cuda.empty_cache()
+
+
+def test_lse_dim0_4x10x32(lib):
+    x = synth.make_inputs("lse_dim0_4x10x32")["x"]
+    out = torch.empty(10, 32, device=DEV)
+    lib.lse_reduce(x.to(DEV), out, 1, 4, 320)
+    assert_parity(out, oracle.logsumexp_dim0(x), "(4,10,32)")
+
+
+def test_log_softmax_256x4096(lib):
+    x = synth.make_inputs("log_softmax_256x4096")["x"]
+    out = torch.empty(256, 4096, device=DEV)
+    lib.log_softmax_lastdim(x.to(DEV), out, 256, 4096)
+    assert_parity(out, oracle.log_softmax(x), "(256,4096)")
+
+
+def test_lse_dim0_32x8192x4096(lib):
+    x = synth.make_inputs("lse_dim0_32x8192x4096", device=DEV)["x"]
+    R, inner = 32, 8192 * 4096
+    out = torch.empty(8192, 4096, device=DEV)
+    lib.lse_reduce(x, out, 1, R, inner)
+    torch.cuda.synchronize()
+    # sampled outputs against the oracle
+    g = torch.Generator().manual_seed(303)
+    idx = torch.randint(0, inner, (8192,), generator=g)
+    idx = torch.cat([idx, torch.tensor([0, 1, 2, 3, inner - 4, inner - 3, inner - 2, inner - 1])])
+    cols = x.view(R, inner)[:, idx.to(DEV)].cpu().contiguous()
+    ref = oracle.lse_reduce(cols, 1, R, cols.shape[1])[0]
+    assert_parity(out.view(-1)[idx.to(DEV)].cpu(), ref, "sampled")
+    # every output: max <= lse <= max + ln R
+    mx = x.view(R, inner).amax(dim=0)
+    o = out.view(-1)
+    assert bool(((o >= mx - 1e-5 * mx.abs()) & (o <= mx + math.log(R) + 1e-5)).all())
+    del x, mx
+
+
+def test_log_softmax_4096x393216(lib):
+    rows, cols = 4096, 393216
+    x = synth.make_inputs("log_softmax_4096x393216", device=DEV)["x"]
+    out = torch.empty_like(x)
+    lib.log_softmax_lastdim(x, out, rows, cols)
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(404)
+    rows_s = sorted(set([0, 1, rows - 1] + torch.randint(0, rows, (9,), generator=g).tolist()))
+    xs = x[rows_s].cpu()
+    assert_parity(out[rows_s].cpu(), oracle.log_softmax(xs), "sampled rows")
+    # every row: sum exp = 1 and out - x constant along the row
+    for r0 in range(0, rows, 512):
+        o = out[r0:r0 + 512].double()
+        s = torch.exp(o).sum(dim=1)
+        assert bool(((s - 1).abs() < 1e-4).all()), float((s - 1).abs().max())
+        d = (x[r0:r0 + 512].double() - o)
+        assert bool(((d - d[:, :1]).abs() < 5e-5).all())
+    del x, out
+
+
+def test_gn_act_lse_128x64x126x126(lib):
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", device=DEV)
+    y, gamma, beta = inp["y"], inp["gamma"], inp["beta"]
+    N, C, H, W = y.shape
+    out = torch.empty(N, 1, H, W, device=DEV)
+    lib.gn_act_lse(y, gamma, beta, out, N, C, H * W, 16, 1e-5)
+    torch.cuda.synchronize()
+    for n in (0, 77, N - 1):
+        ref = oracle.gn_act_lse(y[n:n + 1].cpu(), gamma.cpu(), beta.cpu(), 16, 1e-5)
+        assert_parity(out[n:n + 1].cpu(), ref, f"sample {n}")
+    # every output: max_c r <= out <= max_c r + ln C, with r bounded by y +- 2/3
+    ymax = y.amax(dim=1, keepdim=True)
+    assert bool((out <= ymax + 2.0 / 3.0 + math.log(C) + 1e-4).all())
+    assert bool((out >= ymax - 1.0 / 3.0 - 1e-4).all())

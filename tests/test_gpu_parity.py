@@ -1,0 +1,292 @@
+"""CUDA path against the oracle, element by element, through the C ABI (GPU only).
+
+Sizes here are ones the oracle finishes in seconds but that still span several
+tiles, clusters and a ragged tail; every kernel variant and the special values
+are covered.  Full-size workloads are in test_gpu_fullsize.py.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from log_softmax_gb300 import build
+    build.build()
+    import log_softmax_gb300 as L
+    L.load_library()
+    torch.cuda.set_device(0)
+    yield L
+    assert L.lse_device_status() == 0
+
+
+@pytest.fixture
+def env(monkeypatch):
+    return monkeypatch
+
+
+def _misaligned(t: torch.Tensor) -> torch.Tensor:
+    """Same values at a device address 4 bytes past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 1, dtype=torch.float32, device=DEV)
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def _lse_reduce(L, x_cpu, outer, R, inner, misalign=False):
+    x = x_cpu.to(DEV)
+    out = torch.full((outer, inner), float("nan"), device=DEV)
+    if misalign:
+        x = _misaligned(x)
+        out = _misaligned(out)
+    L.lse_reduce(x, out, outer, R, inner)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def _log_softmax(L, x_cpu, misalign=False):
+    rows, cols = x_cpu.shape
+    x = x_cpu.to(DEV)
+    out = torch.full((rows, cols), float("nan"), device=DEV)
+    if misalign:
+        x = _misaligned(x)
+        out = _misaligned(out)
+    L.log_softmax_lastdim(x, out, rows, cols)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+# ----------------------------------------------------------------------------- form 1
+
+LSE_SHAPES = [
+    (1, 4, 320),        # the (4, 10, 32) task, flattened
+    (1, 32, 4096),      # 32 x 4096 slice of the large strided case
+    (3, 17, 33),        # ragged inner, outer > 1
+    (2, 7, 1000),
+    (1, 1, 64),         # R = 1: lse is x itself
+    (1, 5000, 3),       # long R, tiny inner: thread rows split R
+    (4, 300, 8),
+    (1, 9, 4097),       # inner not a multiple of 4: scalar kernel
+    (5, 2000, 1),       # inner = 1: row statistic kernels
+    (2, 70000, 1),      # inner = 1, long rows: streaming row kernel
+]
+
+
+@pytest.mark.parametrize("outer,R,inner", LSE_SHAPES)
+@pytest.mark.parametrize("misalign", [False, True])
+def test_lse_reduce_parity(lib, outer, R, inner, misalign):
+    x = synth.uniform((outer, R, inner), seed=outer * 1000 + R + inner, lo=-20, hi=20)
+    got = _lse_reduce(lib, x, outer, R, inner, misalign)
+    assert_parity(got, oracle.lse_reduce(x, outer, R, inner), f"lse_reduce {outer,R,inner}")
+
+
+def test_lse_dim0_small_workload(lib):
+    x = synth.make_inputs("lse_dim0_4x10x32")["x"]
+    got = lib.logsumexp(x.to(DEV), dim=0)
+    assert got.shape == (10, 32)
+    assert_parity(got, oracle.logsumexp_dim0(x), "lse dim0 (4,10,32)")
+
+
+def test_logsumexp_other_dims(lib):
+    x = synth.normal((3, 5, 7, 9), seed=5, var=9.0)
+    for dim in range(4):
+        got = lib.logsumexp(x.to(DEV), dim=dim)
+        ref = torch.logsumexp(x.double(), dim=dim).numpy()
+        assert_parity(got, ref, f"dim {dim}")
+
+
+def test_lse_reduce_special_values(lib):
+    inf, nan = float("inf"), float("nan")
+    cols = [[1.0, nan, 2.0, 0.0], [nan, inf, 0.0, 1.0], [inf, 1.0, -inf, 0.0],
+            [-inf, -inf, -inf, -inf], [-inf, 0.0, -inf, -inf], [-inf, 1.0, 2.0, -inf],
+            [1e30, -1e30, 3.0, 1e30], [-1e30, -1e30, -1e30, -1e30]]
+    x = torch.tensor(cols, dtype=torch.float32).T.contiguous()   # (R=4, inner=8)
+    for R_chunks in (1, 3):  # also with the reduced axis repeated (longer R, same answer + log)
+        xx = x.repeat(R_chunks, 1)
+        got = _lse_reduce(lib, xx.reshape(1, 4 * R_chunks, 8), 1, 4 * R_chunks, 8)
+        ref = oracle.lse_reduce(xx, 1, 4 * R_chunks, 8)
+        assert_parity(got, ref, "special")
+
+
+def test_lse_reduce_constant(lib):
+    for R in (1, 3, 32, 257):
+        x = torch.full((2, R, 12), 3.25)
+        got = _lse_reduce(lib, x, 2, R, 12)
+        assert_parity(got, np.full((2, 12), 3.25 + math.log(R)), f"const R={R}")
+
+
+# ----------------------------------------------------------------------------- form 2
+
+LSM_COLS = [1, 3, 4, 5, 31, 32, 33, 127, 128, 129, 512, 1000, 1023, 2048, 4096, 4097, 8192,
+            16384, 16385, 32768, 32769, 32772, 60000, 131072, 393216]
+
+
+@pytest.mark.parametrize("cols", LSM_COLS)
+def test_log_softmax_parity(lib, cols):
+    rows = max(2, min(37, 2_000_000 // cols))
+    x = synth.normal((rows, cols), seed=cols, var=4.0)
+    x.masked_fill_(synth.bernoulli_mask((rows, cols), seed=cols + 1, p=0.01), float("-inf"))
+    x[:, 0] = 0.5  # no row is entirely -inf
+    got = _log_softmax(lib, x)
+    assert_parity(got, oracle.log_softmax(x), f"log_softmax cols={cols}")
+
+
+@pytest.mark.parametrize("cols", [5, 129, 4097, 16385, 70001])
+def test_log_softmax_misaligned(lib, cols):
+    rows = 9
+    x = synth.normal((rows, cols), seed=cols + 7)
+    got = _log_softmax(lib, x, misalign=True)
+    assert_parity(got, oracle.log_softmax(x), f"misaligned cols={cols}")
+
+
+def test_log_softmax_small_workload(lib):
+    x = synth.make_inputs("log_softmax_256x4096")["x"]
+    got = _log_softmax(lib, x)
+    assert_parity(got, oracle.log_softmax(x), "log_softmax (256,4096)")
+
+
+@pytest.mark.parametrize("variant,cluster,threads,chunk", [
+    ("2", "", "", ""), ("2", "1", "", ""), ("2", "2", "", ""), ("2", "4", "", ""),
+    ("2", "8", "", ""), ("2", "16", "", ""), ("2", "", "256", ""), ("2", "", "1024", "2048"),
+    ("2", "8", "1024", "16384"), ("3", "", "", ""),
+])
+def test_log_softmax_variants(lib, env, variant, cluster, threads, chunk):
+    """Each long-row kernel configuration, several rows per cluster so that the
+    persistent loop refills its shared-memory buffers."""
+    env.setenv("LSE_LSM_VARIANT", variant)
+    env.setenv("LSE_LSM_CLUSTER", cluster)
+    env.setenv("LSE_LSM_THREADS", threads)
+    env.setenv("LSE_LSM_CHUNK", chunk)
+    rows, cols = 300, 65536 + 4
+    x = synth.normal((rows, cols), seed=99)
+    got = _log_softmax(lib, x)
+    assert_parity(got, oracle.log_softmax(x), f"variant {variant} CL={cluster} T={threads}")
+
+
+@pytest.mark.parametrize("cluster", ["1", "2", "4", "8"])
+def test_stream_cluster_sizes(lib, env, cluster):
+    env.setenv("LSE_LSM_VARIANT", "3")
+    env.setenv("LSE_STREAM_CLUSTER", cluster)
+    x = synth.normal((5, 100003), seed=3)
+    assert_parity(_log_softmax(lib, x), oracle.log_softmax(x), f"stream CL={cluster}")
+    y = synth.normal((3, 100000), seed=4)
+    got = _lse_reduce(lib, y.reshape(3, 100000, 1), 3, 100000, 1)
+    assert_parity(got.reshape(-1), oracle.row_lse(y), f"row lse CL={cluster}")
+
+
+def test_log_softmax_special_rows(lib):
+    inf, nan = float("inf"), float("nan")
+    for cols in (8, 4096, 40000, 393216):
+        x = synth.normal((6, cols), seed=cols)
+        x[0, 3] = -inf
+        x[1, 5] = inf
+        x[2, 7] = nan
+        x[3, :] = -inf
+        x[4, :] = 7.0
+        x[5, 1] = 1e30
+        got = _log_softmax(lib, x)
+        assert_parity(got, oracle.log_softmax(x), f"special rows cols={cols}")
+
+
+def test_log_softmax_shift_and_normalisation(lib):
+    x = synth.normal((16, 50000), seed=21)
+    a = _log_softmax(lib, x).double()
+    b = _log_softmax(lib, x + 1000.0).double()
+    assert torch.allclose(torch.exp(a).sum(1), torch.ones(16, dtype=torch.float64), atol=1e-5)
+    assert (a - b).abs().max() < 2e-3  # x + 1000 rounds x to ~6e-5 in fp32
+
+
+# ----------------------------------------------------------------------------- form 3
+
+GN_CASES = [
+    (2, 64, 12, 12, 16),
+    (2, 64, 126, 126, 16),   # two samples of the full chain shape
+    (3, 8, 5, 7, 4),         # HW = 35, not a multiple of 4: scalar kernels
+    (2, 6, 4, 4, 3),
+    (1, 4, 1, 1, 1),
+    (2, 32, 9, 9, 32),       # one channel per group
+    (1, 20, 33, 3, 5),       # C not a multiple of 8: channel tail
+]
+
+
+@pytest.mark.parametrize("N,C,H,W,G", GN_CASES)
+def test_gn_act_lse_parity(lib, N, C, H, W, G):
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))
+    got = lib.gn_act_lse_forward(inp["y"].to(DEV), inp["gamma"].to(DEV), inp["beta"].to(DEV), G, 1e-5)
+    ref = oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], G, 1e-5)
+    assert_parity(got, ref, f"gn {N,C,H,W,G}")
+
+
+def test_gn_act_lse_wide_range(lib):
+    """Large gamma and shifted data: z spans about [-60, 60] (tanh saturates),
+    a non-zero mean exercises the statistics."""
+    N, C, H, W, G = 2, 16, 20, 20, 4
+    y = synth.normal((N, C, H, W), seed=77, mean=30.0, var=25.0)
+    gamma = synth.uniform((C,), seed=78, lo=-12.0, hi=12.0)
+    beta = synth.normal((C,), seed=79, var=4.0)
+    got = lib.gn_act_lse_forward(y.to(DEV), gamma.to(DEV), beta.to(DEV), G, 1e-3)
+    assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-3), "gn wide")
+
+
+def test_gn_act_lse_constant_group(lib):
+    """Zero variance in a group: z = beta exactly (eps keeps rstd finite)."""
+    y = torch.full((1, 4, 3, 3), 2.0)
+    gamma = torch.ones(4)
+    beta = torch.tensor([0.0, 0.5, -1.0, 2.0])
+    got = lib.gn_act_lse_forward(y.to(DEV), gamma.to(DEV), beta.to(DEV), 2, 1e-5)
+    assert_parity(got, oracle.gn_act_lse(y, gamma, beta, 2, 1e-5), "gn constant")
+
+
+def test_gn_act_lse_misaligned(lib):
+    N, C, H, W, G = 2, 8, 4, 8, 2
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))
+    y = _misaligned(inp["y"].to(DEV))
+    out = _misaligned(torch.empty(N, 1, H, W, device=DEV))
+    lib.gn_act_lse(y, inp["gamma"].to(DEV), inp["beta"].to(DEV), out, N, C, H * W, G, 1e-5)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu(), oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], G, 1e-5),
+                  "gn misaligned")
+
+
+# ----------------------------------------------------------------------------- streams, host API
+
+def test_side_stream_and_host_tensors(lib):
+    x = synth.normal((64, 5000), seed=1)
+    s = torch.cuda.Stream()
+    xd = x.to(DEV)
+    out = torch.empty_like(xd)
+    with torch.cuda.stream(s):
+        lib.log_softmax_lastdim(xd, out, 64, 5000, stream=s)
+    s.synchronize()
+    assert_parity(out.cpu(), oracle.log_softmax(x), "side stream")
+    got = lib.log_softmax(x.pin_memory())   # host in, host out
+    assert not got.is_cuda
+    assert_parity(got, oracle.log_softmax(x), "host tensors")
+
+
+def test_repeat_calls_are_deterministic(lib):
+    x = synth.normal((40, 393216), seed=11, device=DEV)
+    a = torch.empty_like(x)
+    b = torch.empty_like(x)
+    lib.log_softmax_lastdim(x, a, 40, 393216)
+    lib.log_softmax_lastdim(x, b, 40, 393216)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_log_softmax_persistent_long_rows(lib):
+    """More rows than resident clusters: each cluster loops over rows and refills
+    its shared-memory slice while writing the previous row."""
+    x = synth.normal((64, 393216), seed=12)
+    assert_parity(_log_softmax(lib, x), oracle.log_softmax(x), "64 x 393216")
