@@ -66,11 +66,14 @@ __device__ __forceinline__ void ms_fold(MS& st, const float (&v)[K]) {
         st.s *= f;
         st.m = mn;
     }
-    // shift in base-2 units; an all -inf pair uses shift 0 so -inf - 0 = -inf -> 0
-    float sh = (st.m == -CUDART_INF_F) ? 0.f : st.m * kLog2e;
+    // exp(v - m) = 2^((v - m) * log2 e).  The difference is taken first: it is exact
+    // for v near m, whereas folding m into an fma shift would carry the rounding
+    // error of m * log2 e (about 1e23 when |m| = 1e30).  An all -inf pair uses
+    // base 0, so -inf - 0 = -inf contributes 0.
+    const float base = (st.m == -CUDART_INF_F) ? 0.f : st.m;
     float acc = 0.f;
 #pragma unroll
-    for (int k = 0; k < K; ++k) acc += ex2(fmaf(v[k], kLog2e, -sh));
+    for (int k = 0; k < K; ++k) acc += ex2((v[k] - base) * kLog2e);
     st.s += acc;
 }
 

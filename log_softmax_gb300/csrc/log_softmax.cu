@@ -100,12 +100,12 @@ __global__ void __launch_bounds__(1024) rows_reg_kernel(const float* __restrict_
             __syncthreads();
             m = warp_max_nan(lane < nwarps ? red[lane] : -CUDART_INF_F);
         }
-        const float sh = isfinite(m) ? m * kLog2e : 0.f;
+        const float base = isfinite(m) ? m : 0.f;  // see ms_fold on why v - m comes first
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) s += ex2(fmaf(v[k][e], kLog2e, -sh));
+            for (int e = 0; e < VEC; ++e) s += ex2((v[k][e] - base) * kLog2e);
         s = warp_sum(s);
         if (nwarps > 1) {
             __syncthreads();
