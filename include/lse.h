@@ -108,6 +108,29 @@ lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, f
                         int64_t N, int64_t C, int64_t HW, int64_t G, float eps,
                         cudaStream_t stream);
 
+/*
+ * gn_act_lse_noalloc — the same computation and arguments as gn_act_lse, for
+ * callers that must not allocate device memory: a plugin or engine whose host
+ * framework has reserved all device memory and forbids its components to
+ * allocate, or a latency-critical path that cannot take an allocation's cost or
+ * its out-of-memory failure mid-step.  (The pages have no counterpart: it is a
+ * deployment variant of gn_act_lse.)
+ *   - Allocates nothing: the 2*N*G floats of statistics live in a fixed array
+ *     compiled into the library (512 KiB, N*G <= 65536), which every GPU that
+ *     loads the library holds until the process exits.  N*G > 65536 returns
+ *     LSE_ERR_SIZE; every other argument rule is gn_act_lse's.
+ *   - The first call on a device does a one-time set-up on that device (it looks
+ *     up the array's device address with cudaGetSymbolAddress); make that first
+ *     call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents.  Each call overwrites every entry it reads, so nothing needs
+ *     clearing, but calls whose kernels may overlap on the GPU (different streams
+ *     without ordering) race on it: order them.
+ */
+lse_status_t gn_act_lse_noalloc(const float* y, const float* gamma, const float* beta, float* out,
+                                int64_t N, int64_t C, int64_t HW, int64_t G, float eps,
+                                cudaStream_t stream);
+
 /* Returns the idle memory of the library's scratch pools to the device. */
 lse_status_t lse_release_workspace(void);
 

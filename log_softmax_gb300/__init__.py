@@ -56,6 +56,8 @@ def load_library(path: str = LIB_PATH):
     lib.lse_reduce.argtypes = [vp, vp, i64, i64, i64, vp]
     lib.log_softmax_lastdim.argtypes = [vp, vp, i64, i64, vp]
     lib.gn_act_lse.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
+    lib.gn_act_lse_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
+    lib.gn_act_lse_noalloc.restype = ctypes.c_int
     lib.lse_release_workspace.argtypes = []
     lib.lse_device_status.argtypes = [vp]
     lib.lse_status_string.argtypes = [ctypes.c_int]
@@ -138,6 +140,18 @@ def gn_act_lse(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: float,
         rc = lib.gn_act_lse(_ptr(y), _ptr(gamma), _ptr(beta), _ptr(out), int(N), int(C), int(HW),
                             int(G), float(eps), _stream(stream, y))
     _check("gn_act_lse", rc)
+
+
+def gn_act_lse_noalloc(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: float,
+                       stream=None) -> None:
+    """gn_act_lse for callers that must not allocate device memory: the statistics
+    use a fixed array inside the library (N*G <= 65536; calls on one device share it,
+    so calls that may overlap on the GPU must be ordered)."""
+    lib = load_library()
+    with _device_of(y):
+        rc = lib.gn_act_lse_noalloc(_ptr(y), _ptr(gamma), _ptr(beta), _ptr(out), int(N), int(C),
+                                    int(HW), int(G), float(eps), _stream(stream, y))
+    _check("gn_act_lse_noalloc", rc)
 
 
 def lse_release_workspace() -> None:

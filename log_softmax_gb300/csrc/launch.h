@@ -47,4 +47,7 @@ constexpr int64_t kGnMaxChannels = 8192;
 // Reads an integer tuning knob from the environment (default when unset).
 int env_int(const char* name, int dflt);
 
+// Stores `e` as the calling thread's lse_last_cuda_error() value.
+void record_cuda_error(cudaError_t e);
+
 }  // namespace lse

@@ -86,6 +86,9 @@ bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace
+
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
 }  // namespace lse
 
 using namespace lse;
