@@ -59,7 +59,7 @@ def algorithmic_bytes(w: synth.Workload) -> int:
 # Kernels each step launches (the dominant kernel first).
 LAUNCHES = {
     "lse_dim0": ["lse_strided_kernel"],
-    "log_softmax": ["lsm_smem_cluster_kernel"],
+    "log_softmax": ["lsm_ws_kernel"],
     "gn_act_lse": ["gn_apply_kernel", "gn_stats_kernel"],
 }
 
@@ -247,31 +247,30 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def time_oracle(w: synth.Workload, x_host, budget_s: float, max_units: int, unit_rows: int):
-    """Runs the oracle over successive slices of the sample until budget_s has
-    passed (or max_units slices are done).  Returns (bytes, seconds, units, what)."""
+def time_oracle(w: synth.Workload, x_host, budget_s: float, unit_rows: int):
+    """Runs the oracle over successive slices of the sample, cycling through the
+    sample, until budget_s has passed.  Returns (bytes, seconds, slices done)."""
     import oracle
+    n_units = {"log_softmax": lambda: x_host.shape[0] // unit_rows,
+               "lse_dim0": lambda: x_host.shape[1] // unit_rows,
+               "gn_act_lse": lambda: x_host[0].shape[0] // unit_rows}[w.op]()
+    n_units = max(1, n_units)
     t0 = time.perf_counter()
     done_bytes = 0
     units = 0
-    while units < max_units:
+    while True:
+        k = units % n_units
         if w.op == "log_softmax":
-            sl = x_host[units * unit_rows:(units + 1) * unit_rows]
-            if sl.shape[0] == 0:
-                break
+            sl = x_host[k * unit_rows:(k + 1) * unit_rows]
             oracle.log_softmax(sl)
             done_bytes += 8 * sl.numel()
         elif w.op == "lse_dim0":
-            sl = x_host[:, units * unit_rows:(units + 1) * unit_rows].contiguous()
-            if sl.shape[1] == 0:
-                break
+            sl = x_host[:, k * unit_rows:(k + 1) * unit_rows].contiguous()
             oracle.lse_reduce(sl, 1, sl.shape[0], sl.shape[1])
             done_bytes += 4 * (sl.numel() + sl.shape[1])
         else:
             y, g, b = x_host
-            sl = y[units * unit_rows:(units + 1) * unit_rows]
-            if sl.shape[0] == 0:
-                break
+            sl = y[k * unit_rows:(k + 1) * unit_rows]
             oracle.gn_act_lse(sl, g, b, w.params["G"], w.params["eps"])
             done_bytes += 4 * (sl.numel() + sl.shape[0] * sl.shape[2] * sl.shape[3])
         units += 1
@@ -449,10 +448,10 @@ def run_ours(args, w: synth.Workload):
         import oracle
         oracle.build()
         sample, unit_rows = oracle_sample(w, inputs, 256)
-        b, s, units = time_oracle(w, sample, budget_s=10.0, max_units=256, unit_rows=unit_rows)
-        what = {"log_softmax": f"{units} rows x {w.shape[1]} (first rows of the workload)",
-                "lse_dim0": f"R={w.shape[0]} x {units * 4096} columns (first columns)",
-                "gn_act_lse": f"{units} samples of [64,126,126] (first samples)"}[w.op]
+        b, s, units = time_oracle(w, sample, budget_s=args.cpu_seconds, unit_rows=unit_rows)
+        what = {"log_softmax": f"{units} row passes over the first {sample.shape[0] if hasattr(sample, 'shape') else 0} rows x {w.shape[1]}",
+                "lse_dim0": f"{units} passes of R={w.shape[0]} x 4096 columns over the first {sample.shape[1] if hasattr(sample, 'shape') else 0} columns",
+                "gn_act_lse": f"{units} sample passes over the first {sample[0].shape[0] if isinstance(sample, tuple) else 0} samples of [64,126,126]"}[w.op]
         cpu = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": what + f", {s:.1f} s single-threaded"}
 
@@ -531,10 +530,17 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--shape", default=None,
+                    help="comma-separated shape: the workload's recipe at another size "
+                         "(smaller cases for profiling; not a bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     w = synth.WORKLOADS[args.workload]
+    if args.shape:
+        shape = tuple(int(v) for v in args.shape.split(","))
+        w = synth.Workload(w.name + "@" + "x".join(map(str, shape)), w.op, shape, w.recipe, w.params)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

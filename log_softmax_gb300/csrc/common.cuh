@@ -56,10 +56,20 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b) {
 // exponential per value.  v may hold -inf (it contributes 0) and NaN (it makes
 // m NaN).
 template <int K>
-__device__ __forceinline__ void ms_fold(MS& st, const float (&v)[K]) {
-    float cm = v[0];
+__device__ __forceinline__ float max_nan_tree(const float (&v)[K]) {
+    float t[K];
 #pragma unroll
-    for (int k = 1; k < K; ++k) cm = max_nan(cm, v[k]);
+    for (int k = 0; k < K; ++k) t[k] = v[k];
+#pragma unroll
+    for (int w = 1; w < K; w *= 2)
+#pragma unroll
+        for (int k = 0; k + w < K; k += 2 * w) t[k] = max_nan(t[k], t[k + w]);
+    return t[0];
+}
+
+template <int K>
+__device__ __forceinline__ void ms_fold(MS& st, const float (&v)[K]) {
+    const float cm = max_nan_tree(v);
     float mn = max_nan(st.m, cm);
     if (mn != st.m) {  // also taken once m is NaN; s is NaN from then on anyway
         float f = (st.m == -CUDART_INF_F) ? 0.f : ex2((st.m - mn) * kLog2e);
@@ -71,10 +81,13 @@ __device__ __forceinline__ void ms_fold(MS& st, const float (&v)[K]) {
     // error of m * log2 e (about 1e23 when |m| = 1e30).  An all -inf pair uses
     // base 0, so -inf - 0 = -inf contributes 0.
     const float base = (st.m == -CUDART_INF_F) ? 0.f : st.m;
-    float acc = 0.f;
+    float acc0 = 0.f, acc1 = 0.f;  // two chains for more instructions in flight
 #pragma unroll
-    for (int k = 0; k < K; ++k) acc += ex2((v[k] - base) * kLog2e);
-    st.s += acc;
+    for (int k = 0; k < K; k += 2) {
+        acc0 += ex2((v[k] - base) * kLog2e);
+        if (k + 1 < K) acc1 += ex2((v[k + 1] - base) * kLog2e);
+    }
+    st.s += acc0 + acc1;
 }
 
 // lse from the final pair, with the special-value rules: NaN, then +inf, then
@@ -86,16 +99,31 @@ __device__ __forceinline__ float ms_lse(MS st) {
     return st.m + logf(st.s);
 }
 
-// Warp-wide merge (butterfly, every lane ends with the result).
-__device__ __forceinline__ MS ms_warp_allreduce(MS st) {
+// Rescale factor that brings a pair with max m to the reference max mr >= m:
+// e^(m - mr); an empty pair (m = -inf) contributes 0.
+__device__ __forceinline__ float ms_scale_to(float m, float mr) {
+    return (m == -CUDART_INF_F) ? 0.f : ((m == mr) ? 1.f : ex2((m - mr) * kLog2e));
+}
+
+__device__ __forceinline__ float warp_allmax_nan(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        MS other;
-        other.m = __shfl_xor_sync(0xffffffffu, st.m, o);
-        other.s = __shfl_xor_sync(0xffffffffu, st.s, o);
-        st = ms_merge(st, other);
-    }
-    return st;
+    for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Warp-wide merge, every lane ends with the result: the max first, then each
+// lane rescales its sum once, then a plain sum (one exponential per lane
+// instead of two per butterfly step).
+__device__ __forceinline__ MS ms_warp_allreduce(MS st) {
+    const float m = warp_allmax_nan(st.m);
+    const float s = warp_allsum(st.s * ms_scale_to(st.m, m));
+    return MS{m, s};
 }
 
 // Block-wide merge; every thread gets the result.  `scratch` holds >= 32 MS.
@@ -109,8 +137,7 @@ __device__ __forceinline__ MS ms_block_allreduce(MS st, MS* scratch) {
     if (lane == 0) scratch[warp] = st;
     __syncthreads();
     MS r = (lane < nwarps) ? scratch[lane] : ms_empty();
-    r = ms_warp_allreduce(r);
-    return r;
+    return ms_warp_allreduce(r);
 }
 
 // ---------------------------------------------------------------- memory
@@ -126,6 +153,28 @@ __device__ __forceinline__ float4 ld_stream_f4(const float* p) {
 __device__ __forceinline__ float ld_stream_f1(const float* p) {
     float v;
     asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// L2 eviction policies for loads: keep a line for a re-read soon after, or let
+// it go first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ float4 ld_f4_l2hint(const float* p, uint64_t policy) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(policy));
     return v;
 }
 
@@ -186,6 +235,53 @@ __device__ __forceinline__ MS ld_peer_ms(const MS* local_addr, uint32_t rank) {
     return r;
 }
 
+// ---------------------------------------------------------------- gpu-scope flags
+
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A pair packed into one 64-bit word for a single-copy-atomic hand-over through
+// global memory: low half the max, high half the sum with its lowest bit
+// replaced by a 1-bit tag (relative change of the sum <= 2^-23; when the max is
+// not finite the sum is not used).
+__device__ __forceinline__ unsigned long long ms_pack_tagged(MS v, uint32_t tag) {
+    const uint32_t sb = (__float_as_uint(v.s) & ~1u) | (tag & 1u);
+    return ((unsigned long long)sb << 32) | __float_as_uint(v.m);
+}
+
+__device__ __forceinline__ uint32_t ms_tag_of(unsigned long long w) { return (uint32_t)(w >> 32) & 1u; }
+
+__device__ __forceinline__ MS ms_unpack(unsigned long long w) {
+    return MS{__uint_as_float((uint32_t)w), __uint_as_float((uint32_t)(w >> 32))};
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_ms(MS* p, MS v) {
+    asm volatile("st.relaxed.gpu.global.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(v.m), "f"(v.s) : "memory");
+}
+
+__device__ __forceinline__ MS ld_relaxed_gpu_ms(const MS* p) {
+    MS v;
+    asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.m), "=f"(v.s) : "l"(p) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- mbarrier + bulk copy
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -198,6 +294,16 @@ __device__ __forceinline__ void fence_mbar_init() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among `count` threads (a multiple of 32) of the CTA on hardware
+// barrier `id` (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -240,6 +346,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     atomicExch(status, kStatusTimeout);
     return false;
 }
+
+// Bulk copy (TMA, non-tensor) of `bytes` from this CTA's shared memory to
+// global memory, tracked by the issuing thread's bulk async-groups.  Addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until all of this thread's bulk groups are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Bulk copy (TMA, non-tensor) of `bytes` from global to this CTA's shared
 // memory, completing on `bar` by transaction count.  Addresses 16-byte

@@ -30,6 +30,36 @@ cudaError_t launch_rows_reg(const DeviceInfo& dev, const float* x, float* out, i
 cudaError_t launch_lsm_smem_cluster(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
                                     int64_t cols, cudaStream_t stream);
 
+// Form 2, rows staged in shared memory across a group of CTAs of a cooperative
+// grid (all SMs usable, unlike clusters, which GPC boundaries constrain); the
+// CTAs of a row merge their partial pairs through global memory.  plan_* sizes
+// the launch and its scratch (tagged partial slots); launch_* initialises the
+// slots on `stream` and launches.  cudaErrorNotSupported when the row cannot
+// be staged.
+struct GroupPlan {
+    int threads = 0, nbuf = 1, group_size = 0, groups = 0, slice = 0, chunk = 0;
+    size_t smem = 0, scratch_bytes = 0;
+};
+cudaError_t plan_lsm_smem_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
+                                int64_t cols, GroupPlan* plan);
+cudaError_t launch_lsm_smem_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
+                                  int64_t cols, const GroupPlan& plan, void* scratch,
+                                  cudaStream_t stream);
+
+// Form 2, warp-specialised group kernel (fold warps and store warps on two
+// buffers).  Same plan / scratch protocol.
+cudaError_t plan_lsm_ws_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
+                              int64_t cols, GroupPlan* plan);
+cudaError_t launch_lsm_ws_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
+                                int64_t cols, const GroupPlan& plan, void* scratch, cudaStream_t stream);
+
+// Form 2, rows split over a group of CTAs of a cooperative grid that read their
+// slices twice, the second time from L2.  Same plan / scratch protocol.
+cudaError_t plan_lsm_l2_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
+                              int64_t cols, GroupPlan* plan);
+cudaError_t launch_lsm_l2_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
+                                int64_t cols, const GroupPlan& plan, void* scratch, cudaStream_t stream);
+
 // Form 2, any row length: each CTA of a cluster streams its slice of the row
 // (stats pass, then for mode 0 an apply pass).  mode as for launch_rows_reg.
 cudaError_t launch_rows_stream(const DeviceInfo& dev, const float* x, float* out, int64_t rows,

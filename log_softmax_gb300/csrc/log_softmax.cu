@@ -27,7 +27,9 @@
 // running sum rescaled when the max grows, pairs merged as
 // m = max(m1, m2), s = s1 e^(m1-m) + s2 e^(m2-m)).
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -36,17 +38,6 @@ namespace lse {
 
 // ------------------------------------------------------------------ helpers
 
-__device__ __forceinline__ float warp_max_nan(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 __device__ __forceinline__ float lse_from_max_sum(float m, float s) {
     if (isnan(m)) return CUDART_NAN_F;
@@ -93,12 +84,12 @@ __global__ void __launch_bounds__(1024) rows_reg_kernel(const float* __restrict_
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) m = max_nan(m, v[k][e]);
-        m = warp_max_nan(m);
+        m = warp_allmax_nan(m);
         if (nwarps > 1) {
             __syncthreads();
             if (lane == 0) red[warp] = m;
             __syncthreads();
-            m = warp_max_nan(lane < nwarps ? red[lane] : -CUDART_INF_F);
+            m = warp_allmax_nan(lane < nwarps ? red[lane] : -CUDART_INF_F);
         }
         const float base = isfinite(m) ? m : 0.f;  // see ms_fold on why v - m comes first
         float s = 0.f;
@@ -106,12 +97,12 @@ __global__ void __launch_bounds__(1024) rows_reg_kernel(const float* __restrict_
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) s += ex2((v[k][e] - base) * kLog2e);
-        s = warp_sum(s);
+        s = warp_allsum(s);
         if (nwarps > 1) {
             __syncthreads();
             if (lane == 0) red[warp] = s;
             __syncthreads();
-            s = warp_sum(lane < nwarps ? red[lane] : 0.f);
+            s = warp_allsum(lane < nwarps ? red[lane] : 0.f);
         }
         const float lse = lse_from_max_sum(m, s);
         if constexpr (MODE == 0) {
@@ -189,56 +180,194 @@ struct SmemLayout {
     size_t bytes;   // dynamic shared memory per CTA
 };
 
-__host__ __device__ inline size_t smem_cluster_bytes(int slice) {
-    // [slice floats][kSmemMaxChunks mbarriers][2 MS partials][32 MS scratch][lse + pad]
-    return (size_t)slice * 4 + kSmemMaxChunks * 8 + 2 * sizeof(MS) + 32 * sizeof(MS) + 16;
+__host__ __device__ inline size_t smem_cluster_bytes(int slice, int nbuf = 1) {
+    // [nbuf x slice floats][nbuf x kSmemMaxChunks mbarriers][2 MS partials][32 MS scratch][lse + pad]
+    return (size_t)nbuf * ((size_t)slice * 4 + kSmemMaxChunks * 8) + 2 * sizeof(MS) + 32 * sizeof(MS) + 16;
 }
 
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS, 1) lsm_smem_cluster_kernel(
-    const float* __restrict__ x, float* __restrict__ out, int64_t rows, int64_t cols, int slice,
-    int chunk, int* status) {
+struct SmemRowArgs {
+    const float* x;
+    float* out;
+    int64_t rows, cols;
+    int slice;           // floats of a row owned by one CTA (multiple of 4)
+    int chunk;           // floats per bulk copy (multiple of 4)
+    int* status;         // device status word (bounded-wait timeouts)
+    // group variant only
+    int group_size;            // CTAs per row; CTA b is rank b % group_size of group b / group_size
+    unsigned long long* slots; // [groups][2][group_size] tagged pairs, all bytes 0xFF at launch
+};
+
+// Polls a tagged slot until its tag is `tag`, at most ~1 s / 2^26 polls; on
+// timeout records kStatusTimeout and sets `aborted`.
+__device__ __forceinline__ unsigned long long poll_slot(const unsigned long long* p, uint32_t tag,
+                                                        unsigned long long w, bool& aborted, int* status) {
+    if (ms_tag_of(w) == tag || aborted) return w;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        __nanosleep(20);
+        w = ld_relaxed_gpu_u64(p);
+        if (ms_tag_of(w) == tag) return w;
+        if ((it & 255u) == 255u && globaltimer_ns() - t0 > 1000000000ull) break;
+    }
+    aborted = true;
+    atomicExch(status, kStatusTimeout);
+    return w;
+}
+
+// Rows staged in shared memory, one slice per CTA, the CTAs of a row merging
+// their (m, s) pairs either through distributed shared memory (GROUP = false:
+// the CTAs of a thread-block cluster) or through global memory (GROUP = true:
+// group_size CTAs of a cooperative grid, through tagged slots).
+// Persistent: a group / cluster walks rows first, first + count, ...
+//
+// NBUF = 1: per row, fold the slice as its chunks land, merge (arrive + wait),
+// write x - lse chunk by chunk, refilling each chunk with the next row.
+// NBUF >= 2 (split phase): NBUF slices per CTA.  Step j folds row j, then waits
+// for the merge of row j-1 (whose arrival was one fold earlier, so a straggler
+// in the group costs nothing unless it is a whole row late), arrives for row j
+// and writes row j-1, refilling its buffer with row j+1.  Because every CTA
+// arrives for row j only after its wait for row j-1, no CTA is more than one
+// arrival ahead: two tagged partial slots per CTA suffice.  Writing row j-1
+// refills its buffer with row j-1+NBUF, so with NBUF = 3 the copies run two
+// rows ahead: while row j is folded, row j+1 is already landing.
+template <int THREADS, bool GROUP>
+struct RowMerge {
+    MS* part;                   // cluster: this CTA's two partial slots (shared memory)
+    unsigned long long* slots;  // group: this group's [2][GS] tagged slots (global memory)
+    unsigned long long pend;    // group: this lane's prefetched slot word
+    uint32_t rank, GS;
+
+    // Publishes this CTA's pair for step `it` (all threads call; st is the block
+    // pair).  Group: one 64-bit relaxed store of the pair, tagged with the use
+    // count of its slot mod 2 (slot it % 2 is reused two steps later, and no
+    // CTA arrives for step it + 2 before every CTA has read step it).
+    __device__ __forceinline__ void arrive(uint32_t it, const MS& st) {
+        if constexpr (GROUP) {
+            if (threadIdx.x == 0)
+                st_relaxed_gpu_u64(slots + (it & 1u) * GS + rank, ms_pack_tagged(st, (it >> 1) & 1u));
+        } else {
+            if (threadIdx.x == 0) part[it & 1u] = st;
+            asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+        }
+    }
+
+    // Group: lanes 0..GS-1 of warp 0 issue their slot loads for step `it` early
+    // (the result is only needed in wait()).
+    __device__ __forceinline__ void prefetch(uint32_t it) {
+        if constexpr (GROUP) {
+            if (threadIdx.x < GS) pend = ld_relaxed_gpu_u64(slots + (it & 1u) * GS + threadIdx.x);
+        }
+    }
+
+    // Group only, warp 0 only: waits for every CTA's pair of step `it` (after
+    // prefetch(it)) and returns the merged lse in every lane; no block barrier.
+    __device__ __forceinline__ float wait_warp0(uint32_t it, bool& aborted, int* status) {
+        MS mine = ms_empty();
+        if (threadIdx.x < GS) {
+            const unsigned long long* p = slots + (it & 1u) * GS + threadIdx.x;
+            mine = ms_unpack(poll_slot(p, (it >> 1) & 1u, pend, aborted, status));
+        }
+        return ms_lse(ms_warp_allreduce(mine));
+    }
+
+    // Waits for every CTA's pair of step `it` (after prefetch(it)), merges them
+    // (same order in every CTA, so all compute the same lse) and returns the lse
+    // to all threads.
+    __device__ __forceinline__ float wait(uint32_t it, float* lse_sh, bool& aborted, int* status) {
+        if constexpr (GROUP) {
+            if (threadIdx.x < 32) {
+                MS mine = ms_empty();
+                if (threadIdx.x < GS) {
+                    const unsigned long long* p = slots + (it & 1u) * GS + threadIdx.x;
+                    mine = ms_unpack(poll_slot(p, (it >> 1) & 1u, pend, aborted, status));
+                }
+                const MS tot = ms_warp_allreduce(mine);
+                if (threadIdx.x == 0) *lse_sh = ms_lse(tot);
+            }
+        } else {
+            asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+            if (threadIdx.x == 0) {
+                MS tot = ms_empty();
+                for (uint32_t k = 0; k < GS; ++k) tot = ms_merge(tot, ld_peer_ms(&part[it & 1u], k));
+                *lse_sh = ms_lse(tot);
+            }
+        }
+        __syncthreads();
+        return *lse_sh;
+    }
+};
+
+template <int THREADS, bool GROUP, int NBUF>
+__global__ void __launch_bounds__(THREADS, (1024 / THREADS > 0 ? 1024 / THREADS : 1))
+    lsm_smem_kernel(const SmemRowArgs a) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    float* buf = reinterpret_cast<float*>(smem_raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (size_t)slice * 4);
-    MS* part = reinterpret_cast<MS*>(bars + kSmemMaxChunks);
+    const int slice = a.slice, chunk = a.chunk;
+    const int64_t rows = a.rows, cols = a.cols;
+    float* const buf0 = reinterpret_cast<float*>(smem_raw);
+    uint64_t* const bars0 = reinterpret_cast<uint64_t*>(smem_raw + (size_t)NBUF * slice * 4);
+    MS* part = reinterpret_cast<MS*>(bars0 + NBUF * kSmemMaxChunks);
     MS* red = part + 2;
     float* lse_sh = reinterpret_cast<float*>(red + 32);
 
-    const uint32_t rank = cluster_ctarank();
-    const uint32_t CL = cluster_nctarank();
-    const int64_t c_begin = (int64_t)rank * slice;
+    RowMerge<THREADS, GROUP> mg;
+    mg.pend = 0;
+    int64_t first_row, row_step;
+    if constexpr (GROUP) {
+        mg.GS = (uint32_t)a.group_size;
+        mg.rank = blockIdx.x % mg.GS;
+        first_row = blockIdx.x / mg.GS;
+        row_step = gridDim.x / mg.GS;
+        mg.slots = a.slots + first_row * 2 * mg.GS;
+        mg.part = nullptr;
+    } else {
+        mg.rank = cluster_ctarank();
+        mg.GS = cluster_nctarank();
+        first_row = cluster_id_x();
+        row_step = nclusters_x();
+        mg.part = part;
+        mg.slots = nullptr;
+    }
+    const int64_t c_begin = (int64_t)mg.rank * slice;
     const int len = (int)std::max<int64_t>(0, std::min<int64_t>(slice, cols - c_begin));
     const int nch = (len + chunk - 1) / chunk;
-    const int64_t first_row = cluster_id_x();
-    const int64_t row_step = nclusters_x();
     const int tid = threadIdx.x;
+    const int64_t nrows = first_row < rows ? (rows - first_row + row_step - 1) / row_step : 0;
     bool aborted = false;
+    uint32_t filled[NBUF], folded[NBUF];  // rows issued into / folded from each buffer (thread 0)
+#pragma unroll
+    for (int b = 0; b < NBUF; ++b) filled[b] = folded[b] = 0;
 
     if (tid == 0) {
-        for (int c = 0; c < nch; ++c) mbar_init(&bars[c], 1);
+        for (int c = 0; c < NBUF * kSmemMaxChunks; ++c) mbar_init(&bars0[c], 1);
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (tid == 0 && first_row < rows) {
-        const float* src = x + first_row * cols + c_begin;
-        for (int c = 0; c < nch; ++c) {
+    // Copies step j's row (if any) into buffer j % NBUF (thread 0; chunk c only,
+    // or all chunks when c < 0).
+    auto issue = [&](int64_t j, int c_only) {
+        if (j >= nrows || aborted) return;
+        const int b = (int)(j % NBUF);
+        if (c_only <= 0) ++filled[b];
+        const float* src = a.x + (first_row + j * row_step) * cols + c_begin;
+        for (int c = (c_only < 0 ? 0 : c_only); c < (c_only < 0 ? nch : c_only + 1); ++c) {
             const int cb = c * chunk;
             const uint32_t bytes = (uint32_t)std::min(chunk, len - cb) * 4u;
-            mbar_arrive_expect_tx(&bars[c], bytes);
-            bulk_g2s(buf + cb, src + cb, bytes, &bars[c]);
+            if (c_only >= 0) fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars0[b * kSmemMaxChunks + c], bytes);
+            bulk_g2s(buf0 + (size_t)b * slice + cb, src + cb, bytes, &bars0[b * kSmemMaxChunks + c]);
         }
-    }
+    };
 
-    uint32_t it = 0;
-    uint32_t abort_par = 0;
-    for (int64_t row = first_row; row < rows; row += row_step, ++it) {
-        const uint32_t par = it & 1u;
-        // ---- fold the slice into (m, s) as its chunks land
+    // Folds step j's slice into the block pair as its chunks land.
+    auto fold = [&](int64_t j) -> MS {
+        const int b = (int)(j % NBUF);
+        const uint32_t phase = (uint32_t)((j / NBUF) & 1);
+        const float* buf = buf0 + (size_t)b * slice;
+        uint64_t* bars = bars0 + b * kSmemMaxChunks;
         MS st = ms_empty();
         for (int c = 0; c < nch; ++c) {
-            if (!mbar_wait_bounded(&bars[c], par, aborted, status) && abort_par == 0) abort_par = par + 1;
+            mbar_wait_bounded(&bars[c], phase, aborted, a.status);
             const int cb = c * chunk;
             const int n4 = std::min(chunk, len - cb) >> 2;
             const float4* p = reinterpret_cast<const float4*>(buf + cb);
@@ -247,65 +376,250 @@ __global__ void __launch_bounds__(THREADS, 1) lsm_smem_cluster_kernel(
                 float v[16];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    float4 a = p[i + k * THREADS];
-                    v[4 * k + 0] = a.x; v[4 * k + 1] = a.y; v[4 * k + 2] = a.z; v[4 * k + 3] = a.w;
+                    float4 q = p[i + k * THREADS];
+                    v[4 * k + 0] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
                 }
                 ms_fold<16>(st, v);
             }
             for (; i < n4; i += THREADS) {
-                float4 a = p[i];
-                float v[4] = {a.x, a.y, a.z, a.w};
+                float4 q = p[i];
+                float v[4] = {q.x, q.y, q.z, q.w};
                 ms_fold<4>(st, v);
             }
         }
-        st = ms_block_allreduce(st, red);
-        // ---- merge the CTAs' pairs through distributed shared memory
-        if (tid == 0) part[par] = st;
-        cluster_sync();
-        if (tid == 0) {
-            MS tot = ms_empty();
-            for (uint32_t k = 0; k < CL; ++k) tot = ms_merge(tot, ld_peer_ms(&part[par], k));
-            *lse_sh = ms_lse(tot);
-        }
-        __syncthreads();
-        const float lse = *lse_sh;
-        // ---- write x - lse from shared memory; refill each chunk with the next row
-        const int64_t next = row + row_step;
-        float* dst = out + row * cols + c_begin;
-        const float* nsrc = x + next * cols + c_begin;
+        if (!aborted) ++folded[b];
+        return ms_block_allreduce(st, red);
+    };
+
+    // Writes step j's row as x - lse from its buffer; as each chunk is consumed,
+    // copies step j + NBUF's row into it.
+    auto store = [&](int64_t j, float lse) {
+        const int b = (int)(j % NBUF);
+        const float* buf = buf0 + (size_t)b * slice;
+        float* dst = a.out + (first_row + j * row_step) * cols + c_begin;
         for (int c = 0; c < nch; ++c) {
             const int cb = c * chunk;
-            const int clen = std::min(chunk, len - cb);
-            const int n4 = clen >> 2;
+            const int n4 = std::min(chunk, len - cb) >> 2;
             const float4* p = reinterpret_cast<const float4*>(buf + cb);
             for (int i = tid; i < n4; i += THREADS) {
-                float4 a = p[i];
-                st_stream_f4(dst + cb + 4 * i, make_float4(a.x - lse, a.y - lse, a.z - lse, a.w - lse));
+                float4 q = p[i];
+                st_stream_f4(dst + cb + 4 * i, make_float4(q.x - lse, q.y - lse, q.z - lse, q.w - lse));
             }
             __syncthreads();  // every thread is done reading chunk c
-            if (tid == 0 && next < rows && !aborted) {
-                fence_proxy_async_smem();
-                const uint32_t bytes = (uint32_t)clen * 4u;
-                mbar_arrive_expect_tx(&bars[c], bytes);
-                bulk_g2s(buf + cb, nsrc + cb, bytes, &bars[c]);
+            if (tid == 0) issue(j + NBUF, c);
+        }
+    };
+
+    if (tid == 0)
+        for (int j = 0; j < NBUF; ++j) issue(j, -1);
+
+    static_assert(NBUF >= 1 && NBUF <= 3, "one to three buffers");
+    if constexpr (NBUF == 1) {
+        for (int64_t j = 0; j < nrows; ++j) {
+            const MS st = fold(j);
+            mg.arrive((uint32_t)j, st);
+            mg.prefetch((uint32_t)j);
+            const float lse = mg.wait((uint32_t)j, lse_sh, aborted, a.status);
+            store(j, lse);
+        }
+    } else {
+        for (int64_t j = 0; j <= nrows; ++j) {
+            if (j > 0) mg.prefetch((uint32_t)(j - 1));  // in flight during the fold
+            MS st = ms_empty();
+            if (j < nrows) st = fold(j);
+            float lse_prev = 0.f;
+            if (j > 0) lse_prev = mg.wait((uint32_t)(j - 1), lse_sh, aborted, a.status);
+            if (j < nrows) mg.arrive((uint32_t)j, st);
+            if (j > 0) store(j - 1, lse_prev);
+        }
+    }
+
+    if (aborted && tid == 0) {
+        // A copy never completed; none was issued after that.  Give each buffer's
+        // fill still outstanding (at most one per buffer) one more bounded wait
+        // before the CTA releases its shared memory.
+        bool again = false;
+        for (int bb = 0; bb < NBUF; ++bb) {
+            if (filled[bb] <= folded[bb]) continue;
+            for (int c = 0; c < nch; ++c)
+                mbar_wait_bounded(&bars0[bb * kSmemMaxChunks + c], folded[bb] & 1u, again, a.status);
+        }
+    }
+    if constexpr (!GROUP) cluster_sync();  // peers may still read part[] of this CTA
+}
+
+// Slice = ceil(cols / G) rounded up to 32 floats, so that every slice starts on
+// a 128-byte line (neighbouring CTAs never share a line); chunk = floats per
+// bulk copy (at most kSmemMaxChunks per slice).
+// Warp-specialised group kernel, NB buffers per CTA.  FW fold warps fold each
+// row (as its chunks land) and publish the CTA's pair; they never wait for the
+// group.  SW store warps wait for the group's pairs of row j, merge them, write
+// row j out of its buffer and refill each of its chunks with row j+NB.  Store
+// back-pressure and the merge wait then stall only the store warps, while the
+// fold warps run up to NB rows ahead.  A fold warp publishing row r implies
+// every store warp of the group has read row r-2NB (r needs this CTA's store
+// of r-NB, which needed every pair of r-NB, which needed every CTA's store of
+// r-2NB), so kWsSlots = 16 >= 2NB tagged slots per CTA (tag = (r / 16) mod 2)
+// suffice.  Groups of up to 64 CTAs: each lane of the merging warp reads two
+// slots.
+constexpr int kWsSlots = 16;
+constexpr int kWsMaxGroup = 64;
+
+template <int FW, int SW, int NB>
+__global__ void __launch_bounds__(32 * (FW + SW), 1) lsm_ws_kernel(const SmemRowArgs a) {
+    static_assert(2 * NB <= kWsSlots, "slots must cover two rounds of buffers");
+    constexpr int NF = 32 * FW, NS = 32 * SW;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int slice = a.slice, chunk = a.chunk;
+    const int64_t rows = a.rows, cols = a.cols;
+    float* const buf0 = reinterpret_cast<float*>(smem_raw);
+    uint64_t* const full = reinterpret_cast<uint64_t*>(smem_raw + (size_t)NB * slice * 4);  // [NB][K]
+    float* const lse_s = reinterpret_cast<float*>(full + NB * kSmemMaxChunks);              // [1]
+    MS* const red = reinterpret_cast<MS*>(lse_s + 4);                                      // [2][32]
+
+    const uint32_t GS = (uint32_t)a.group_size;
+    const uint32_t rank = blockIdx.x % GS;
+    const int64_t first_row = blockIdx.x / GS;
+    const int64_t row_step = gridDim.x / GS;
+    unsigned long long* const slots = a.slots + first_row * kWsSlots * GS;  // [kWsSlots][GS]
+    const int64_t c_begin = (int64_t)rank * slice;
+    const int len = (int)std::max<int64_t>(0, std::min<int64_t>(slice, cols - c_begin));
+    const int nch = (len + chunk - 1) / chunk;
+    const int64_t nrows = first_row < rows ? (rows - first_row + row_step - 1) / row_step : 0;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    bool aborted = false;
+
+    if (tid == 0) {
+        for (int c = 0; c < NB * kSmemMaxChunks; ++c) mbar_init(&full[c], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Issuer: the first store thread.  Copies step j's row into buffer j % NB.
+    uint32_t filled[NB];
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) filled[bb] = 0;
+    auto issue = [&](int64_t j, int c_only) {
+        if (j >= nrows || aborted) return;
+        const int b = (int)(j % NB);
+        if (c_only <= 0) ++filled[b];
+        const float* src = a.x + (first_row + j * row_step) * cols + c_begin;
+        for (int c = (c_only < 0 ? 0 : c_only); c < (c_only < 0 ? nch : c_only + 1); ++c) {
+            const int cb = c * chunk;
+            const uint32_t bytes = (uint32_t)std::min(chunk, len - cb) * 4u;
+            if (c_only >= 0) fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&full[b * kSmemMaxChunks + c], bytes);
+            bulk_g2s(buf0 + (size_t)b * slice + cb, src + cb, bytes, &full[b * kSmemMaxChunks + c]);
+        }
+    };
+    if (tid == NF)
+        for (int j = 0; j < NB; ++j) issue(j, -1);
+
+    if (warp < FW) {
+        // ---------------- fold warps: fold, reduce, publish; never wait for the group
+        for (int64_t j = 0; j < nrows; ++j) {
+            const int b = (int)(j % NB);
+            const uint32_t phase = (uint32_t)((j / NB) & 1);
+            const float* buf = buf0 + (size_t)b * slice;
+            MS st = ms_empty();
+            for (int c = 0; c < nch; ++c) {
+                mbar_wait_bounded(&full[b * kSmemMaxChunks + c], phase, aborted, a.status);
+                const int cb = c * chunk;
+                const int n4 = std::min(chunk, len - cb) >> 2;
+                const float4* p = reinterpret_cast<const float4*>(buf + cb);
+                int i = tid;
+                for (; i + 3 * NF < n4; i += 4 * NF) {
+                    float v[16];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float4 q = p[i + k * NF];
+                        v[4 * k + 0] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
+                    }
+                    ms_fold<16>(st, v);
+                }
+                for (; i < n4; i += NF) {
+                    float4 q = p[i];
+                    float v[4] = {q.x, q.y, q.z, q.w};
+                    ms_fold<4>(st, v);
+                }
+            }
+            st = ms_warp_allreduce(st);
+            if (lane == 0) red[(j & 1) * 32 + warp] = st;
+            named_bar_sync(1, NF);  // every fold warp is done with this row and its red slot
+            if (warp == 0) {
+                MS r = (lane < FW) ? red[(j & 1) * 32 + lane] : ms_empty();
+                r = ms_warp_allreduce(r);
+                if (lane == 0)
+                    st_relaxed_gpu_u64(slots + (j % kWsSlots) * GS + rank,
+                                       ms_pack_tagged(r, (uint32_t)(j / kWsSlots) & 1u));
+            }
+        }
+    } else {
+        // ---------------- store warps: merge the group's pairs, write, refill
+        const int sid = tid - NF;
+        for (int64_t j = 0; j < nrows; ++j) {
+            const int b = (int)(j % NB);
+            if (sid < 32) {
+                MS mine = ms_empty();
+                for (uint32_t k = (uint32_t)sid; k < GS; k += 32) {
+                    const unsigned long long* p = slots + (j % kWsSlots) * GS + k;
+                    const MS other = ms_unpack(poll_slot(p, (uint32_t)(j / kWsSlots) & 1u,
+                                                         ld_relaxed_gpu_u64(p), aborted, a.status));
+                    mine = ms_merge(mine, other);
+                }
+                const float l = ms_lse(ms_warp_allreduce(mine));
+                if (sid == 0) *lse_s = l;
+            }
+            named_bar_sync(2, NS);  // lse_s holds row j's lse
+            const float lse = *lse_s;
+            const float* buf = buf0 + (size_t)b * slice;
+            float* dst = a.out + (first_row + j * row_step) * cols + c_begin;
+            for (int c = 0; c < nch; ++c) {
+                const int cb = c * chunk;
+                const int n4 = std::min(chunk, len - cb) >> 2;
+                const float4* p = reinterpret_cast<const float4*>(buf + cb);
+                for (int i = sid; i < n4; i += NS) {
+                    float4 q = p[i];
+                    st_stream_f4(dst + cb + 4 * i, make_float4(q.x - lse, q.y - lse, q.z - lse, q.w - lse));
+                }
+                named_bar_sync(2, NS);  // every store warp is done reading chunk c (and lse_s)
+                if (sid == 0) issue(j + NB, c);
             }
         }
     }
-    if (aborted && tid == 0 && abort_par != 0) {
-        // A copy never completed: stop issuing (done above) and give the copies of
-        // the abandoned row one more bounded wait before the CTA releases its
-        // shared memory.
-        bool again = false;
-        for (int c = 0; c < nch; ++c) mbar_wait_bounded(&bars[c], abort_par - 1, again, status);
+    __syncthreads();
+    if (tid == NF) {
+        // After a timeout anywhere, give each buffer's last issued fill one more
+        // bounded wait before the shared memory is released.
+        if (atomicAdd(a.status, 0) != 0) {
+            bool again = false;
+            for (int bb = 0; bb < NB; ++bb) {
+                if (filled[bb] == 0) continue;
+                for (int c = 0; c < nch; ++c)
+                    mbar_wait_bounded(&full[bb * kSmemMaxChunks + c], (filled[bb] - 1) & 1u, again, a.status);
+            }
+        }
     }
-    cluster_sync();  // peers may still read part[] of this CTA
 }
 
-template <int THREADS>
+__host__ inline size_t smem_ws_bytes(int slice, int nb) {
+    return (size_t)nb * slice * 4 + (size_t)nb * kSmemMaxChunks * 8 + 16 + 64 * sizeof(MS);
+}
+
+static void smem_chunking(int64_t cols, int G, int chunk_env, int* slice, int* chunk) {
+    const int64_t sl = ((cols + G - 1) / G + 31) / 32 * 32;
+    *slice = (int)std::min<int64_t>(sl, 1 << 26);
+    int ch = std::min(std::max(1024, chunk_env & ~3), *slice);
+    if ((*slice + ch - 1) / ch > kSmemMaxChunks) ch = ((*slice + kSmemMaxChunks - 1) / kSmemMaxChunks + 3) / 4 * 4;
+    *chunk = ch;
+}
+
+template <int THREADS, int NBUF>
 static cudaError_t smem_cluster_go(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
                                    int64_t cols, int CL, int slice, int chunk, size_t smem,
                                    cudaStream_t stream) {
-    auto kern = lsm_smem_cluster_kernel<THREADS>;
+    auto kern = lsm_smem_kernel<THREADS, false, NBUF>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (CL > 8) {
@@ -330,7 +644,12 @@ static cudaError_t smem_cluster_go(const DeviceInfo& dev, const float* x, float*
     if (max_clusters < 1) return cudaErrorNotSupported;
     const int64_t nclusters = std::min<int64_t>(rows, max_clusters);
     cfg.gridDim = dim3((unsigned)(nclusters * CL));
-    e = cudaLaunchKernelEx(&cfg, kern, x, out, rows, cols, slice, chunk, dev.status);
+    if (env_int("LSE_VERBOSE", 0))
+        fprintf(stderr, "[lse] lsm_smem cluster: CL=%d nbuf=%d threads=%d slice=%d chunk=%d smem=%zu "
+                "max_clusters=%d clusters=%lld\n", CL, NBUF, THREADS, slice, chunk, smem, max_clusters,
+                (long long)nclusters);
+    SmemRowArgs args{x, out, rows, cols, slice, chunk, dev.status, CL, nullptr};
+    e = cudaLaunchKernelEx(&cfg, kern, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -343,26 +662,31 @@ cudaError_t launch_lsm_smem_cluster(const DeviceInfo& dev, const float* x, float
     if (cols % 4 != 0 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
         return cudaErrorNotSupported;
     const int threads = env_int("LSE_LSM_THREADS", 512);
-    int chunk = env_int("LSE_LSM_CHUNK", 8192);
-    chunk = std::max(1024, chunk & ~3);
+    const int chunk_env = env_int("LSE_LSM_CHUNK", 8192);
     const int forced = env_int("LSE_LSM_CLUSTER", 0);
+    const int nbuf = env_int("LSE_LSM_NBUF", 1) == 2 ? 2 : 1;
     const int cands[5] = {1, 2, 4, 8, 16};
     for (int ci = 0; ci < 5; ++ci) {
         const int CL = cands[ci];
         if (forced && CL != forced) continue;
-        const int64_t sl = ((cols + CL - 1) / CL + 3) / 4 * 4;
-        const size_t smem = smem_cluster_bytes((int)std::min<int64_t>(sl, 1 << 26));
-        if (sl > (1 << 26) || smem > (size_t)dev.max_smem_optin) continue;
-        const int slice = (int)sl;
-        int ch = std::min(chunk, slice);
-        if ((slice + ch - 1) / ch > kSmemMaxChunks) ch = ((slice + kSmemMaxChunks - 1) / kSmemMaxChunks + 3) / 4 * 4;
+        int slice, ch;
+        smem_chunking(cols, CL, chunk_env, &slice, &ch);
+        const size_t smem = smem_cluster_bytes(slice, nbuf);
+        if ((int64_t)slice * CL < cols || smem > (size_t)dev.max_smem_optin) continue;
         cudaError_t e;
-        if (threads == 256)
-            e = smem_cluster_go<256>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
+        if (nbuf == 2) {
+            if (threads == 256)
+                e = smem_cluster_go<256, 2>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
+            else if (threads == 1024)
+                e = smem_cluster_go<1024, 2>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
+            else
+                e = smem_cluster_go<512, 2>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
+        } else if (threads == 256)
+            e = smem_cluster_go<256, 1>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
         else if (threads == 1024)
-            e = smem_cluster_go<1024>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
+            e = smem_cluster_go<1024, 1>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
         else
-            e = smem_cluster_go<512>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
+            e = smem_cluster_go<512, 1>(dev, x, out, rows, cols, CL, slice, ch, smem, stream);
         if (e == cudaErrorNotSupported || e == cudaErrorInvalidClusterSize) {
             (void)cudaGetLastError();
             continue;
@@ -370,6 +694,437 @@ cudaError_t launch_lsm_smem_cluster(const DeviceInfo& dev, const float* x, float
         return e;
     }
     return cudaErrorNotSupported;
+}
+
+// ---- group variant: plan (host), then launch with caller-provided scratch
+
+template <int THREADS, int NBUF>
+static cudaError_t group_occupancy(size_t smem, int* per_sm) {
+    auto kern = lsm_smem_kernel<THREADS, true, NBUF>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, THREADS, smem);
+}
+
+static cudaError_t group_occupancy_any(int threads, int nbuf, size_t smem, int* per_sm) {
+    if (nbuf == 3) {
+        return threads == 256 ? group_occupancy<256, 3>(smem, per_sm)
+             : threads == 1024 ? group_occupancy<1024, 3>(smem, per_sm)
+                               : group_occupancy<512, 3>(smem, per_sm);
+    }
+    if (nbuf == 2) {
+        return threads == 256 ? group_occupancy<256, 2>(smem, per_sm)
+             : threads == 1024 ? group_occupancy<1024, 2>(smem, per_sm)
+                               : group_occupancy<512, 2>(smem, per_sm);
+    }
+    return threads == 256 ? group_occupancy<256, 1>(smem, per_sm)
+         : threads == 1024 ? group_occupancy<1024, 1>(smem, per_sm)
+                           : group_occupancy<512, 1>(smem, per_sm);
+}
+
+namespace {
+struct PlanKey {
+    int device;
+    int64_t rows, cols;
+    int threads, chunk, group, nbuf;
+    bool operator==(const PlanKey& o) const {
+        return device == o.device && rows == o.rows && cols == o.cols && threads == o.threads &&
+               chunk == o.chunk && group == o.group && nbuf == o.nbuf;
+    }
+};
+std::mutex g_plan_mu;
+PlanKey g_plan_keys[16];
+GroupPlan g_plans[16];
+int g_plan_n = 0, g_plan_next = 0;
+}  // namespace
+
+// Chooses the group size GS (CTAs per row, 1..32) and the buffering: the plan
+// that keeps the most CTA slots of the GPU busy, preferring deeper buffering
+// (each extra buffer is worth 4 % of coverage) and then the smallest group.
+// LSE_LSM_GROUP forces GS, LSE_LSM_NBUF forces 1, 2 or 3 buffers,
+// LSE_LSM_THREADS (256/512/1024) and LSE_LSM_CHUNK (floats per copy) tune.
+cudaError_t plan_lsm_smem_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
+                                int64_t cols, GroupPlan* plan) {
+    if (cols % 4 != 0 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+        return cudaErrorNotSupported;
+    const int threads = env_int("LSE_LSM_THREADS", 256);
+    const int chunk_env = env_int("LSE_LSM_CHUNK", 8192);
+    const int forced = env_int("LSE_LSM_GROUP", 0);
+    const int nbuf_env = env_int("LSE_LSM_NBUF", 0);
+    const PlanKey key{dev.device, rows, cols, threads, chunk_env, forced, nbuf_env};
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mu);
+        for (int i = 0; i < g_plan_n; ++i)
+            if (g_plan_keys[i] == key) {
+                *plan = g_plans[i];
+                return cudaSuccess;
+            }
+    }
+    double best_score = -1.0;
+    GroupPlan best;
+    for (int nbuf = 3; nbuf >= 1; --nbuf) {
+        if (nbuf_env && nbuf != nbuf_env) continue;
+        for (int GS = 1; GS <= 32; ++GS) {
+            if (forced && GS != forced) continue;
+            int slice, ch;
+            smem_chunking(cols, GS, chunk_env, &slice, &ch);
+            const size_t smem = smem_cluster_bytes(slice, nbuf);
+            if ((int64_t)slice * GS < cols || smem > (size_t)dev.max_smem_optin) continue;
+            if ((int64_t)slice * (GS - 1) >= cols) continue;  // a CTA would own nothing
+            int per_sm = 0;
+            cudaError_t e = group_occupancy_any(threads, nbuf, smem, &per_sm);
+            if (e != cudaSuccess) return e;
+            const int64_t slots = (int64_t)per_sm * dev.sm_count;
+            const int64_t groups = std::min<int64_t>(rows, slots / GS);
+            if (groups < 1) continue;
+            const double cover = (double)(groups * GS) / (double)slots;
+            const double score = cover + 0.04 * (nbuf - 1) - 1e-4 * GS;
+            if (score > best_score) {
+                best_score = score;
+                best.threads = threads;
+                best.nbuf = nbuf;
+                best.group_size = GS;
+                best.groups = (int)groups;
+                best.slice = slice;
+                best.chunk = ch;
+                best.smem = smem;
+                best.scratch_bytes = (size_t)groups * 2 * GS * sizeof(unsigned long long);
+            }
+        }
+    }
+    if (best_score < 0) return cudaErrorNotSupported;
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mu);
+        g_plan_keys[g_plan_next] = key;
+        g_plans[g_plan_next] = best;
+        g_plan_next = (g_plan_next + 1) % 16;
+        g_plan_n = std::min(g_plan_n + 1, 16);
+    }
+    *plan = best;
+    return cudaSuccess;
+}
+
+template <int THREADS, int NBUF>
+static cudaError_t group_go(const SmemRowArgs& args, const GroupPlan& p, cudaStream_t stream) {
+    auto kern = lsm_smem_kernel<THREADS, true, NBUF>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the group waits end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cfg.gridDim = dim3((unsigned)(p.groups * p.group_size));
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lsm_smem_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
+                                  int64_t cols, const GroupPlan& p, void* scratch, cudaStream_t stream) {
+    // every slot starts with tag 1, which no step's first use expects
+    cudaError_t e = cudaMemsetAsync(scratch, 0xFF, p.scratch_bytes, stream);
+    if (e != cudaSuccess) return e;
+    if (env_int("LSE_VERBOSE", 0))
+        fprintf(stderr, "[lse] lsm_smem group: GS=%d groups=%d nbuf=%d threads=%d slice=%d chunk=%d "
+                "smem=%zu\n", p.group_size, p.groups, p.nbuf, p.threads, p.slice, p.chunk, p.smem);
+    SmemRowArgs args{x, out, rows, cols, p.slice, p.chunk, dev.status, p.group_size,
+                     static_cast<unsigned long long*>(scratch)};
+    if (p.nbuf == 3) {
+        if (p.threads == 256) return group_go<256, 3>(args, p, stream);
+        if (p.threads == 1024) return group_go<1024, 3>(args, p, stream);
+        return group_go<512, 3>(args, p, stream);
+    }
+    if (p.nbuf == 2) {
+        if (p.threads == 256) return group_go<256, 2>(args, p, stream);
+        if (p.threads == 1024) return group_go<1024, 2>(args, p, stream);
+        return group_go<512, 2>(args, p, stream);
+    }
+    if (p.threads == 256) return group_go<256, 1>(args, p, stream);
+    if (p.threads == 1024) return group_go<1024, 1>(args, p, stream);
+    return group_go<512, 1>(args, p, stream);
+}
+
+// ---- warp-specialised group variant
+
+template <int FW, int SW, int NB>
+static cudaError_t ws_occupancy(size_t smem, int* per_sm) {
+    auto kern = lsm_ws_kernel<FW, SW, NB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, 32 * (FW + SW), smem);
+}
+
+// Warp splits compiled: (fold, store) = (4,4) (8,4) (8,8) (12,4) (16,4).
+static int ws_split(int fw, int sw) {
+    if (fw == 8 && sw == 4) return 1;
+    if (fw == 8 && sw == 8) return 2;
+    if (fw == 12 && sw == 4) return 3;
+    if (fw == 16 && sw == 4) return 4;
+    return 0;
+}
+
+template <int NB>
+static cudaError_t ws_occupancy_nb(int fw, int sw, size_t smem, int* per_sm) {
+    switch (ws_split(fw, sw)) {
+        case 1: return ws_occupancy<8, 4, NB>(smem, per_sm);
+        case 2: return ws_occupancy<8, 8, NB>(smem, per_sm);
+        case 3: return ws_occupancy<12, 4, NB>(smem, per_sm);
+        case 4: return ws_occupancy<16, 4, NB>(smem, per_sm);
+        default: return ws_occupancy<4, 4, NB>(smem, per_sm);
+    }
+}
+
+static cudaError_t ws_occupancy_any(int nb, int fw, int sw, size_t smem, int* per_sm) {
+    switch (nb) {
+        case 2: return ws_occupancy_nb<2>(fw, sw, smem, per_sm);
+        case 4: return ws_occupancy_nb<4>(fw, sw, smem, per_sm);
+        case 5: return ws_occupancy_nb<5>(fw, sw, smem, per_sm);
+        default: return ws_occupancy_nb<3>(fw, sw, smem, per_sm);
+    }
+}
+
+// Buffers NB (LSE_WS_NB: 2..5, default 3; 0 lets the planner choose) and group
+// size GS (1..64): the plan that covers the most CTA slots (LSE_WS_GROUP forces
+// GS); warps LSE_WS_FW / LSE_WS_SW (default 8 fold, 4 store).
+cudaError_t plan_lsm_ws_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
+                              int64_t cols, GroupPlan* plan) {
+    if (cols % 4 != 0 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+        return cudaErrorNotSupported;
+    int fw = env_int("LSE_WS_FW", 8);
+    int sw = env_int("LSE_WS_SW", 4);
+    if (ws_split(fw, sw) == 0) fw = sw = 4;
+    const int chunk_env = env_int("LSE_LSM_CHUNK", 8192);
+    const int forced = env_int("LSE_WS_GROUP", 0);
+    const int nb_env = env_int("LSE_WS_NB", 3);
+    double best_score = -1.0;
+    for (int nb = 5; nb >= 2; --nb) {
+        if (nb_env && nb != nb_env) continue;
+        for (int GS = 1; GS <= kWsMaxGroup; ++GS) {
+            if (forced && GS != forced) continue;
+            int slice, ch;
+            smem_chunking(cols, GS, chunk_env, &slice, &ch);
+            const size_t smem = smem_ws_bytes(slice, nb);
+            if ((int64_t)slice * GS < cols || smem > (size_t)dev.max_smem_optin) continue;
+            if ((int64_t)slice * (GS - 1) >= cols) continue;
+            int per_sm = 0;
+            cudaError_t e = ws_occupancy_any(nb, fw, sw, smem, &per_sm);
+            if (e != cudaSuccess) return e;
+            const int64_t slots = (int64_t)per_sm * dev.sm_count;
+            const int64_t groups = std::min<int64_t>(rows, slots / GS);
+            if (groups < 1) continue;
+            // Coverage of the SM slots, minus a cost per CTA of the group (smaller
+            // slices and a wider merge: GS = 38 ran 25 % slower than GS = 24 on
+            // 393,216-float rows), plus a bonus when the slices split the row
+            // exactly on 4 KiB boundaries (equal work for every CTA of a group).
+            const bool even = (cols % ((int64_t)GS * 1024) == 0);
+            const double score = (double)(groups * GS) / (double)slots - 0.004 * GS + (even ? 0.05 : 0.0) +
+                                 0.03 * (nb - 2);
+            if (score > best_score) {
+                best_score = score;
+                plan->threads = 32 * (fw + sw);
+                plan->nbuf = nb * 10000 + fw * 100 + sw;  // records buffers and the warp split
+                plan->group_size = GS;
+                plan->groups = (int)groups;
+                plan->slice = slice;
+                plan->chunk = ch;
+                plan->smem = smem;
+                plan->scratch_bytes = (size_t)groups * kWsSlots * GS * sizeof(unsigned long long);
+            }
+        }
+    }
+    return best_score < 0 ? cudaErrorNotSupported : cudaSuccess;
+}
+
+template <int FW, int SW, int NB>
+static cudaError_t ws_go(const SmemRowArgs& args, const GroupPlan& p, cudaStream_t stream) {
+    auto kern = lsm_ws_kernel<FW, SW, NB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the group waits end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(32 * (FW + SW));
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cfg.gridDim = dim3((unsigned)(p.groups * p.group_size));
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int NB>
+static cudaError_t ws_go_nb(int fw, int sw, const SmemRowArgs& args, const GroupPlan& p,
+                            cudaStream_t stream) {
+    switch (ws_split(fw, sw)) {
+        case 1: return ws_go<8, 4, NB>(args, p, stream);
+        case 2: return ws_go<8, 8, NB>(args, p, stream);
+        case 3: return ws_go<12, 4, NB>(args, p, stream);
+        case 4: return ws_go<16, 4, NB>(args, p, stream);
+        default: return ws_go<4, 4, NB>(args, p, stream);
+    }
+}
+
+cudaError_t launch_lsm_ws_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
+                                int64_t cols, const GroupPlan& p, void* scratch, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(scratch, 0xFF, p.scratch_bytes, stream);
+    if (e != cudaSuccess) return e;
+    const int nb = p.nbuf / 10000, fw = (p.nbuf / 100) % 100, sw = p.nbuf % 100;
+    if (env_int("LSE_VERBOSE", 0))
+        fprintf(stderr, "[lse] lsm_ws group: GS=%d groups=%d buffers=%d fold_warps=%d store_warps=%d "
+                "slice=%d chunk=%d smem=%zu\n", p.group_size, p.groups, nb, fw, sw, p.slice, p.chunk, p.smem);
+    SmemRowArgs args{x, out, rows, cols, p.slice, p.chunk, dev.status, p.group_size,
+                     static_cast<unsigned long long*>(scratch)};
+    switch (nb) {
+        case 2: return ws_go_nb<2>(fw, sw, args, p, stream);
+        case 4: return ws_go_nb<4>(fw, sw, args, p, stream);
+        case 5: return ws_go_nb<5>(fw, sw, args, p, stream);
+        default: return ws_go_nb<3>(fw, sw, args, p, stream);
+    }
+}
+
+// ------------------------------------------------------------------ rows re-read from L2 by a group
+
+// Each CTA of a group owns a slice of the row.  Pass 1 streams the slice from
+// HBM into the running pair with loads that ask L2 to keep the lines; the
+// group merges its pairs through tagged slots; pass 2 reads the slice again
+// (from L2: the slices in flight across the GPU are sized to fit in it) and
+// writes x - lse with streaming stores.  HBM sees one read and one write, and
+// several CTAs per SM hide each other's merge waits.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS) lsm_l2_group_kernel(const float* __restrict__ x,
+                                                               float* __restrict__ out, int64_t rows,
+                                                               int64_t cols, int group_size, int slice,
+                                                               unsigned long long* slots, int* status) {
+    __shared__ MS red[32];
+    __shared__ float lse_sh;
+    constexpr int T = THREADS;
+    RowMerge<THREADS, true> mg;
+    mg.GS = (uint32_t)group_size;
+    mg.rank = blockIdx.x % mg.GS;
+    const int64_t g = blockIdx.x / mg.GS;
+    const int64_t NG = gridDim.x / mg.GS;
+    mg.slots = slots + g * 2 * mg.GS;
+    mg.part = nullptr;
+    mg.pend = 0;
+    const int64_t c_begin = (int64_t)mg.rank * slice;
+    const int64_t len = std::max<int64_t>(0, std::min<int64_t>(slice, cols - c_begin));
+    const int64_t n4 = len >> 2;
+    const int tid = threadIdx.x;
+    const uint64_t keep = l2_policy_evict_last();
+    const uint64_t drop = l2_policy_evict_first();
+    bool aborted = false;
+    uint32_t j = 0;
+    for (int64_t row = g; row < rows; row += NG, ++j) {
+        const float* src = x + row * cols + c_begin;
+        MS st = ms_empty();
+        int64_t i = tid;
+        for (; i + 3 * T < n4; i += 4 * T) {
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 q = ld_f4_l2hint(src + 4 * (i + k * T), keep);
+                v[4 * k + 0] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
+            }
+            ms_fold<16>(st, v);
+        }
+        for (; i < n4; i += T) {
+            const float4 q = ld_f4_l2hint(src + 4 * i, keep);
+            float v[4] = {q.x, q.y, q.z, q.w};
+            ms_fold<4>(st, v);
+        }
+        st = ms_block_allreduce(st, red);
+        mg.arrive(j, st);
+        mg.prefetch(j);
+        const float lse = mg.wait(j, &lse_sh, aborted, status);
+        float* dst = out + row * cols + c_begin;
+        i = tid;
+        for (; i + 3 * T < n4; i += 4 * T) {
+            float4 q[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q[k] = ld_f4_l2hint(src + 4 * (i + k * T), drop);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                st_stream_f4(dst + 4 * (i + k * T),
+                             make_float4(q[k].x - lse, q[k].y - lse, q[k].z - lse, q[k].w - lse));
+        }
+        for (; i < n4; i += T) {
+            const float4 q = ld_f4_l2hint(src + 4 * i, drop);
+            st_stream_f4(dst + 4 * i, make_float4(q.x - lse, q.y - lse, q.z - lse, q.w - lse));
+        }
+    }
+}
+
+template <int THREADS>
+static cudaError_t l2_occupancy(int* per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lsm_l2_group_kernel<THREADS>, THREADS, 0);
+}
+
+// Group size LSE_L2_GROUP (default 16), CTA size LSE_L2_THREADS (256 / 512 / 1024,
+// default 512).  Needs 16-byte-aligned rows.
+cudaError_t plan_lsm_l2_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
+                              int64_t cols, GroupPlan* plan) {
+    if (cols % 4 != 0 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+        return cudaErrorNotSupported;
+    const int threads = env_int("LSE_L2_THREADS", 512);
+    int GS = std::min(32, std::max(1, env_int("LSE_L2_GROUP", 16)));
+    int per_sm = 0;
+    cudaError_t e = threads == 256 ? l2_occupancy<256>(&per_sm)
+                  : threads == 1024 ? l2_occupancy<1024>(&per_sm)
+                                    : l2_occupancy<512>(&per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t groups = std::min<int64_t>(rows, (int64_t)per_sm * dev.sm_count / GS);
+    if (groups < 1) return cudaErrorNotSupported;
+    const int64_t sl = ((cols + GS - 1) / GS + 31) / 32 * 32;
+    if (sl > (int64_t)1 << 30) return cudaErrorNotSupported;
+    plan->threads = threads;
+    plan->nbuf = 0;
+    plan->group_size = GS;
+    plan->groups = (int)groups;
+    plan->slice = (int)sl;
+    plan->chunk = 0;
+    plan->smem = 0;
+    plan->scratch_bytes = (size_t)groups * 2 * GS * sizeof(unsigned long long);
+    return cudaSuccess;
+}
+
+template <int THREADS>
+static cudaError_t l2_go(const DeviceInfo& dev, const float* x, float* out, int64_t rows, int64_t cols,
+                         const GroupPlan& p, unsigned long long* slots, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the group waits end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.gridDim = dim3((unsigned)(p.groups * p.group_size));
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lsm_l2_group_kernel<THREADS>, x, out, rows, cols,
+                                       p.group_size, p.slice, slots, dev.status);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lsm_l2_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
+                                int64_t cols, const GroupPlan& p, void* scratch, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(scratch, 0xFF, p.scratch_bytes, stream);
+    if (e != cudaSuccess) return e;
+    if (env_int("LSE_VERBOSE", 0))
+        fprintf(stderr, "[lse] lsm_l2 group: GS=%d groups=%d threads=%d slice=%d\n", p.group_size,
+                p.groups, p.threads, p.slice);
+    auto* slots = static_cast<unsigned long long*>(scratch);
+    if (p.threads == 256) return l2_go<256>(dev, x, out, rows, cols, p, slots, stream);
+    if (p.threads == 1024) return l2_go<1024>(dev, x, out, rows, cols, p, slots, stream);
+    return l2_go<512>(dev, x, out, rows, cols, p, slots, stream);
 }
 
 // ------------------------------------------------------------------ rows streamed by a cluster

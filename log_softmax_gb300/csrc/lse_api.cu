@@ -133,12 +133,35 @@ lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64
     lse_status_t st = device_state(&s);
     if (st != LSE_OK) return st;
     cudaError_t e;
-    const int force = env_int("LSE_LSM_VARIANT", 0);  // 1 registers, 2 cluster smem, 3 streaming
-    if ((force == 0 && cols <= kRegRowMaxCols) || (force == 1 && cols <= kRegRowMaxCols)) {
+    // LSE_LSM_VARIANT forces a kernel: 1 registers, 2 cluster shared memory,
+    // 3 streaming, 4 lock-step group shared memory, 5 group with an L2 re-read,
+    // 6 warp-specialised group shared memory (the default for long aligned rows).
+    const int force = env_int("LSE_LSM_VARIANT", 0);
+    if ((force == 0 || force == 1) && cols <= kRegRowMaxCols) {
         e = launch_rows_reg(s->info, x, out, rows, cols, 0, stream);
     } else {
         e = cudaErrorNotSupported;
-        if (force == 0 || force == 2) e = launch_lsm_smem_cluster(s->info, x, out, rows, cols, stream);
+        if (force == 2) {
+            e = launch_lsm_smem_cluster(s->info, x, out, rows, cols, stream);
+        } else if (force == 0 || force == 4 || force == 5 || force == 6) {
+            const int kind = force == 0 ? 6 : force;
+            GroupPlan plan;
+            e = kind == 5 ? plan_lsm_l2_group(s->info, x, out, rows, cols, &plan)
+              : kind == 6 ? plan_lsm_ws_group(s->info, x, out, rows, cols, &plan)
+                          : plan_lsm_smem_group(s->info, x, out, rows, cols, &plan);
+            if (e == cudaSuccess) {
+                cudaMemPool_t pool = nullptr;
+                if ((st = device_pool(s, &pool)) != LSE_OK) return st;
+                void* scratch = nullptr;
+                e = cudaMallocFromPoolAsync(&scratch, plan.scratch_bytes, pool, stream);
+                if (e != cudaSuccess) return cuda_fail(e);
+                e = kind == 5 ? launch_lsm_l2_group(s->info, x, out, rows, cols, plan, scratch, stream)
+                  : kind == 6 ? launch_lsm_ws_group(s->info, x, out, rows, cols, plan, scratch, stream)
+                              : launch_lsm_smem_group(s->info, x, out, rows, cols, plan, scratch, stream);
+                cudaError_t ef = cudaFreeAsync(scratch, stream);
+                if (e == cudaSuccess) e = ef;
+            }
+        }
         if (e == cudaErrorNotSupported) {
             (void)cudaGetLastError();
             e = launch_rows_stream(s->info, x, out, rows, cols, 0, stream);

@@ -98,9 +98,10 @@ def make_inputs(w: Workload | str, device="cpu", shape=None):
         w = WORKLOADS[w]
     shape = tuple(shape) if shape is not None else w.shape
     p = w.params
-    if w.name.startswith("lse_dim0_4x10x32"):
+    base = w.name.split("@")[0]
+    if base == "lse_dim0_4x10x32":
         return {"x": normal(shape, p["seed"], device=device)}
-    if w.name.startswith("log_softmax_256x4096"):
+    if base == "log_softmax_256x4096":
         x = normal(shape, p["seed"], var=4.0, device=device)
         mask = bernoulli_mask(shape, p["mask_seed"], p["p_ninf"], device=device)
         x.masked_fill_(mask, float("-inf"))
@@ -109,11 +110,11 @@ def make_inputs(w: Workload | str, device="cpu", shape=None):
             if bool(all_ninf.any()):
                 raise RuntimeError("recipe produced an all -inf row; pick another seed")
         return {"x": x}
-    if w.name.startswith("lse_dim0_32x8192x4096"):
+    if base == "lse_dim0_32x8192x4096":
         return {"x": uniform(shape, p["seed"], -20.0, 20.0, device=device)}
-    if w.name.startswith("log_softmax_4096x393216"):
+    if base == "log_softmax_4096x393216":
         return {"x": normal(shape, p["seed"], device=device)}
-    if w.name.startswith("gn_act_lse"):
+    if base == "gn_act_lse_128x64x126x126":
         C = shape[1]
         return {
             "y": normal(shape, p["seed"], device=device),

@@ -156,22 +156,68 @@ def test_log_softmax_small_workload(lib):
     assert_parity(got, oracle.log_softmax(x), "log_softmax (256,4096)")
 
 
-@pytest.mark.parametrize("variant,cluster,threads,chunk", [
-    ("2", "", "", ""), ("2", "1", "", ""), ("2", "2", "", ""), ("2", "4", "", ""),
-    ("2", "8", "", ""), ("2", "16", "", ""), ("2", "", "256", ""), ("2", "", "1024", "2048"),
-    ("2", "8", "1024", "16384"), ("3", "", "", ""),
-])
-def test_log_softmax_variants(lib, env, variant, cluster, threads, chunk):
-    """Each long-row kernel configuration, several rows per cluster so that the
-    persistent loop refills its shared-memory buffers."""
-    env.setenv("LSE_LSM_VARIANT", variant)
-    env.setenv("LSE_LSM_CLUSTER", cluster)
-    env.setenv("LSE_LSM_THREADS", threads)
-    env.setenv("LSE_LSM_CHUNK", chunk)
+LONG_ROW_CONFIGS = [
+    # cluster shared memory (DSMEM merge)
+    {"LSE_LSM_VARIANT": "2"}, {"LSE_LSM_VARIANT": "2", "LSE_LSM_CLUSTER": "1"},
+    {"LSE_LSM_VARIANT": "2", "LSE_LSM_CLUSTER": "2"}, {"LSE_LSM_VARIANT": "2", "LSE_LSM_CLUSTER": "4"},
+    {"LSE_LSM_VARIANT": "2", "LSE_LSM_CLUSTER": "8"}, {"LSE_LSM_VARIANT": "2", "LSE_LSM_CLUSTER": "16"},
+    {"LSE_LSM_VARIANT": "2", "LSE_LSM_THREADS": "256"},
+    {"LSE_LSM_VARIANT": "2", "LSE_LSM_THREADS": "1024", "LSE_LSM_CHUNK": "2048"},
+    {"LSE_LSM_VARIANT": "2", "LSE_LSM_CLUSTER": "8", "LSE_LSM_THREADS": "1024", "LSE_LSM_CHUNK": "16384"},
+    {"LSE_LSM_VARIANT": "2", "LSE_LSM_NBUF": "2"},
+    {"LSE_LSM_VARIANT": "2", "LSE_LSM_NBUF": "2", "LSE_LSM_CLUSTER": "4", "LSE_LSM_THREADS": "256"},
+    {"LSE_LSM_VARIANT": "2", "LSE_LSM_NBUF": "2", "LSE_LSM_CLUSTER": "16", "LSE_LSM_CHUNK": "2048"},
+    # streaming
+    {"LSE_LSM_VARIANT": "3"},
+    # group shared memory (global-memory merge), single and double buffered
+    {"LSE_LSM_VARIANT": "4"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_NBUF": "1"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_NBUF": "2"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "2", "LSE_LSM_NBUF": "1"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "3", "LSE_LSM_NBUF": "2"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "5"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "8", "LSE_LSM_NBUF": "1"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "19", "LSE_LSM_NBUF": "2"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "32"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_NBUF": "3"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_NBUF": "3", "LSE_LSM_GROUP": "6", "LSE_LSM_CHUNK": "2048"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_NBUF": "3", "LSE_LSM_GROUP": "24", "LSE_LSM_THREADS": "512"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "8", "LSE_LSM_THREADS": "512", "LSE_LSM_CHUNK": "4096"},
+    # warp-specialised group
+    {"LSE_LSM_VARIANT": "6"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_GROUP": "2"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_GROUP": "7", "LSE_WS_FW": "8", "LSE_WS_NB": "2"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_GROUP": "16", "LSE_WS_SW": "8", "LSE_LSM_CHUNK": "2048"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_FW": "8", "LSE_WS_SW": "8"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "2"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "2", "LSE_WS_GROUP": "5", "LSE_WS_FW": "8"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "3", "LSE_WS_GROUP": "24", "LSE_WS_SW": "8"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "3", "LSE_WS_GROUP": "3", "LSE_LSM_CHUNK": "2048"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "4", "LSE_WS_GROUP": "40", "LSE_WS_FW": "12"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "5", "LSE_WS_GROUP": "38", "LSE_WS_FW": "16"},
+    {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "0", "LSE_WS_FW": "4", "LSE_WS_SW": "4"},
+    # group with an L2 re-read
+    {"LSE_LSM_VARIANT": "5"},
+    {"LSE_LSM_VARIANT": "5", "LSE_L2_GROUP": "1"},
+    {"LSE_LSM_VARIANT": "5", "LSE_L2_GROUP": "3", "LSE_L2_THREADS": "256"},
+    {"LSE_LSM_VARIANT": "5", "LSE_L2_GROUP": "32", "LSE_L2_THREADS": "1024"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "16", "LSE_LSM_THREADS": "1024", "LSE_LSM_CHUNK": "2048"},
+    {"LSE_LSM_VARIANT": "4", "LSE_LSM_GROUP": "2", "LSE_LSM_THREADS": "512", "LSE_LSM_CHUNK": "16384",
+     "LSE_LSM_NBUF": "1"},
+]
+
+
+@pytest.mark.parametrize("cfg", LONG_ROW_CONFIGS,
+                         ids=["-".join(f"{k[8:]}{v}" for k, v in c.items()) for c in LONG_ROW_CONFIGS])
+def test_log_softmax_variants(lib, env, cfg):
+    """Each long-row kernel configuration, several rows per cluster / group so that
+    the persistent loop refills its shared-memory buffers."""
+    for k, v in cfg.items():
+        env.setenv(k, v)
     rows, cols = 300, 65536 + 4
     x = synth.normal((rows, cols), seed=99)
     got = _log_softmax(lib, x)
-    assert_parity(got, oracle.log_softmax(x), f"variant {variant} CL={cluster} T={threads}")
+    assert_parity(got, oracle.log_softmax(x), f"config {cfg}")
 
 
 @pytest.mark.parametrize("cluster", ["1", "2", "4", "8"])
