@@ -17,6 +17,7 @@
 //                    channel plane; the channel lse is kept online as a
 //                    (max, sum) pair per pixel, one rescale per 8 channels.
 #include <algorithm>
+#include <cstdio>
 
 #include "common.cuh"
 #include "launch.h"
@@ -119,18 +120,83 @@ __global__ void __launch_bounds__(512) gn_stats_kernel(const float* __restrict__
 
 // ------------------------------------------------------------------ fused apply + channel lse
 
-// tanh(z) = sign(z) * (1 - 2 / (e^(2|z|) + 1)); absolute error ~2e-7, which is
-// what the residual r = y + hardswish(tanh(z)) needs (|d hardswish / dt| <= 5/6).
-__device__ __forceinline__ float tanh_ex2(float z) {
-    const float e = ex2(fabsf(z) * (2.f * kLog2e));
-    return copysignf(1.f - __fdividef(2.f, e + 1.f), z);
+// tanh from u = 2 z log2(e):  tanh(z) = sign(z) * (1 - 2 / (2^|u| + 1)), with the
+// hardware base-2 exponential and approximate reciprocal; absolute error ~2e-7,
+// which is what the residual r = y + hardswish(tanh(z)) needs
+// (|d hardswish / dt| <= 5/6 on [-1, 1]).  The result lies in [-1, 1] (or NaN).
+__device__ __forceinline__ float tanh_from_u(float u) {
+    const float e = ex2(fabsf(u));
+    float q;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(q) : "f"(e + 1.f));
+    return copysignf(fmaf(-2.f, q, 1.f), u);
 }
 
-__device__ __forceinline__ float act_residual(float v, float mean, float scale, float shift) {
-    const float z = fmaf(v - mean, scale, shift);
-    const float t = tanh_ex2(z);
-    const float h = t * fminf(fmaxf(t + 3.f, 0.f), 6.f) * (1.f / 6.f);
-    return v + h;
+// r = y + hardswish(tanh(z)) with z = (v - mean) * rstd * gamma + beta, from the
+// table entry e = {mean, rstd * gamma * 2 log2(e), beta * 2 log2(e), 0}.
+// HardSwish is t * min(max(t + 3, 0), 6) / 6; for t in [-1, 1] the clamp never
+// binds (t + 3 lies in [2, 4]), so it equals t * (t / 6 + 1/2), and a NaN t
+// gives NaN either way.
+__device__ __forceinline__ float act_residual(float v, float4 e) {
+    const float u = fmaf(v - e.x, e.y, e.z);
+    const float t = tanh_from_u(u);
+    return fmaf(t, fmaf(t, 1.f / 6.f, 0.5f), v);
+}
+
+// VEC floats at p; with HINT, 128-bit loads carry the L2 eviction `policy`.
+template <int VEC, bool HINT = false>
+__device__ __forceinline__ void load_vec(const float* p, float (&v)[VEC], uint64_t policy = 0) {
+    if constexpr (VEC == 4) {
+        const float4 a = HINT ? ld_f4_l2hint(p, policy) : ld_stream_f4(p);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
+        v[0] = ld_stream_f1(p);
+    }
+}
+
+// One thread's VEC adjacent pixels of one sample: loop over the C channel planes
+// (each load a coalesced read across the warp), normalise / activate / add the
+// residual, keep the channel lse online per pixel (one rescale per CH channels)
+// and write the VEC results.  tab[c] = {mean, rstd*gamma*2log2e, beta*2log2e, 0}.
+template <int VEC, bool HINT = false, int CH = 8>
+__device__ __forceinline__ void apply_pixels(const float* __restrict__ yp, const float4* tab, int C,
+                                             int64_t HW, float* __restrict__ dst, uint64_t policy = 0) {
+    MS st[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) st[j] = ms_empty();
+    int c = 0;
+    for (; c + CH <= C; c += CH) {
+        float r[VEC][CH];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            float v[VEC];
+            load_vec<VEC, HINT>(yp + (int64_t)(c + k) * HW, v, policy);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) r[j][k] = v[j];
+        }
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const float4 e = tab[c + k];
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) r[j][k] = act_residual(r[j][k], e);
+        }
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) ms_fold<CH>(st[j], r[j]);
+    }
+    for (; c < C; ++c) {
+        float v[VEC];
+        load_vec<VEC, HINT>(yp + (int64_t)c * HW, v, policy);
+        const float4 e = tab[c];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            float r[1] = {act_residual(v[j], e)};
+            ms_fold<1>(st[j], r);
+        }
+    }
+    if constexpr (VEC == 4) {
+        *reinterpret_cast<float4*>(dst) = make_float4(ms_lse(st[0]), ms_lse(st[1]), ms_lse(st[2]), ms_lse(st[3]));
+    } else {
+        dst[0] = ms_lse(st[0]);
+    }
 }
 
 template <int VEC>
@@ -140,9 +206,8 @@ __global__ void __launch_bounds__(128) gn_apply_kernel(const float* __restrict__
                                                        const float* __restrict__ stats,
                                                        float* __restrict__ out, int64_t N, int C,
                                                        int64_t HW, int G, int64_t tiles) {
-    extern __shared__ float tab[];  // [C] mean, [C] rstd*gamma, [C] beta for the current sample
+    extern __shared__ float4 tab[];  // [C] {mean, rstd*gamma*2log2e, beta*2log2e, 0} of the sample
     constexpr int T = 128;
-    constexpr int CH = 8;
     const int tid = threadIdx.x;
     const int cpg = C / G;
     int64_t cur_n = -1;
@@ -155,63 +220,166 @@ __global__ void __launch_bounds__(128) gn_apply_kernel(const float* __restrict__
                 const int g = c / cpg;
                 const float mean = stats[2 * (n * G + g)];
                 const float rstd = stats[2 * (n * G + g) + 1];
-                tab[c] = mean;
-                tab[C + c] = rstd * gamma[c];
-                tab[2 * C + c] = beta[c];
+                tab[c] = make_float4(mean, rstd * gamma[c] * (2.f * kLog2e), beta[c] * (2.f * kLog2e), 0.f);
             }
             __syncthreads();
             cur_n = n;
         }
         const int64_t p0 = (tile * T + tid) * VEC;
         if (p0 >= HW) continue;
-        const float* yp = y + n * (int64_t)C * HW + p0;
-        MS st[VEC];
+        apply_pixels<VEC>(y + n * (int64_t)C * HW + p0, tab, C, HW, out + n * HW + p0);
+    }
+}
+
+// ------------------------------------------------------------------ one-kernel chain with an L2 re-read
+
+// Welford of base[lo, hi) (VEC-wide loads; lo, hi multiples of VEC) merged over
+// the block; every thread gets the result.  Loads ask L2 to keep the lines.
+template <int VEC, int T>
+__device__ __forceinline__ Welford block_welford(const float* __restrict__ base, int64_t lo, int64_t hi,
+                                                 uint64_t policy, Welford* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    Welford w{0.f, 0.f, 0.f};
+    const int64_t nv = (hi - lo) / VEC;
+    const float* b = base + lo;
+    int64_t i = tid;
+    for (; i + 3 * T < nv; i += 4 * T) {
+        float v[4 * VEC];
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) st[j] = ms_empty();
-        int c = 0;
-        for (; c + CH <= C; c += CH) {
-            float r[VEC][CH];
+        for (int k = 0; k < 4; ++k) {
+            float q[VEC];
+            load_vec<VEC, true>(b + (i + k * T) * VEC, q, policy);
 #pragma unroll
-            for (int k = 0; k < CH; ++k) {
-                const float* p = yp + (int64_t)(c + k) * HW;
-                if constexpr (VEC == 4) {
-                    float4 a = ld_stream_f4(p);
-                    r[0][k] = a.x; r[1][k] = a.y; r[2][k] = a.z; r[3][k] = a.w;
-                } else {
-                    r[0][k] = ld_stream_f1(p);
+            for (int e = 0; e < VEC; ++e) v[k * VEC + e] = q[e];
+        }
+        w = wf_merge(w, wf_batch<4 * VEC>(v));
+    }
+    for (; i < nv; i += T) {
+        float q[VEC];
+        load_vec<VEC, true>(b + i * VEC, q, policy);
+        w = wf_merge(w, wf_batch<VEC>(q));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w = wf_merge(w, wf_shfl_xor(w, o));
+    __syncthreads();
+    if (lane == 0) red[warp] = w;
+    __syncthreads();
+    Welford r = (lane < T / 32) ? red[lane] : Welford{0.f, 0.f, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = wf_merge(r, wf_shfl_xor(r, o));
+    return r;
+}
+
+struct GnFusedArgs {
+    const float* y;
+    const float* gamma;
+    const float* beta;
+    float* out;
+    int64_t N, HW;
+    int C, G, parts, tiles, lag;
+    float eps;
+    float4* partials;          // [N][G][parts] (count, mean, M2, -)
+    unsigned* done;            // [N] statistics parts finished, zero at launch
+    unsigned long long* next;  // work-item counter, zero at launch
+    int* status;
+};
+
+// Work items are claimed from one counter in a fixed order: for k = 0, 1, ...:
+// the statistics parts of sample k (G * parts items), then the apply tiles of
+// sample k - lag.  An apply tile waits (bounded) until every statistics part of
+// its sample is done; those parts were claimed earlier by CTAs that are running
+// (the grid is cooperative: all CTAs resident) and wait on nothing, so the wait
+// ends.  The lag keeps each sample's second read close behind its first, while
+// the sample (4 MB at 64 x 126 x 126) is still in L2: HBM sees y once.
+template <int VEC>
+__global__ void __launch_bounds__(256) gn_fused_kernel(const GnFusedArgs a) {
+    constexpr int T = 256;
+    extern __shared__ float4 tab[];  // [C] {mean, rstd*gamma*2log2e, beta*2log2e, 0}
+    __shared__ Welford red[32];
+    __shared__ long long item_sh;
+    const int tid = threadIdx.x;
+    const int C = a.C, G = a.G, P = a.parts, cpg = C / G;
+    const int64_t N = a.N, HW = a.HW;
+    const int64_t GP = (int64_t)G * P, TT = a.tiles;
+    const int64_t lag = a.lag;
+    const int64_t total = N * (GP + TT);
+    const uint64_t keep = l2_policy_evict_last();
+    const uint64_t drop = l2_policy_evict_first();
+    bool aborted = false;
+    for (;;) {
+        if (tid == 0) item_sh = (long long)atomicAdd(a.next, 1ull);
+        __syncthreads();
+        const int64_t t = item_sh;
+        __syncthreads();
+        if (t >= total) break;
+        // t -> (statistics part or apply tile, sample n, index within the sample)
+        bool is_stats;
+        int64_t n, idx;
+        if (t < lag * GP) {
+            is_stats = true;
+            n = t / GP;
+            idx = t - n * GP;
+        } else if (t < lag * GP + (N - lag) * (GP + TT)) {
+            const int64_t u = t - lag * GP;
+            const int64_t k = lag + u / (GP + TT);
+            const int64_t r = u - (k - lag) * (GP + TT);
+            is_stats = r < GP;
+            n = is_stats ? k : k - lag;
+            idx = is_stats ? r : r - GP;
+        } else {
+            const int64_t u = t - lag * GP - (N - lag) * (GP + TT);
+            n = N - lag + u / TT;
+            idx = u - (n - (N - lag)) * TT;
+            is_stats = false;
+        }
+        if (is_stats) {
+            const int64_t g = idx / P, p = idx - (idx / P) * P;
+            const int64_t nv = (int64_t)cpg * HW / VEC;
+            const int64_t lo = (nv * p / P) * VEC, hi = (nv * (p + 1) / P) * VEC;
+            const Welford w = block_welford<VEC, T>(a.y + (n * C + g * cpg) * HW, lo, hi, keep, red);
+            if (tid == 0) {
+                float4* dst = a.partials + (n * G + g) * P + p;
+                asm volatile("st.relaxed.gpu.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(w.n),
+                             "f"(w.mean), "f"(w.m2), "f"(0.f)
+                             : "memory");
+                red_release_gpu_add(a.done + n, 1u);
+            }
+        } else {
+            if (tid == 0 && !aborted && ld_acquire_gpu_u32(a.done + n) < (unsigned)GP) {
+                const uint64_t t0 = globaltimer_ns();
+                bool ok = false;
+                for (uint32_t it = 0; it < (1u << 26); ++it) {
+                    __nanosleep(64);
+                    if (ld_acquire_gpu_u32(a.done + n) >= (unsigned)GP) {
+                        ok = true;
+                        break;
+                    }
+                    if ((it & 255u) == 255u && globaltimer_ns() - t0 > 1000000000ull) break;
+                }
+                if (!ok) {
+                    aborted = true;
+                    atomicExch(a.status, kStatusTimeout);
                 }
             }
-#pragma unroll
-            for (int k = 0; k < CH; ++k) {
-                const float mean = tab[c + k], sc = tab[C + c + k], sh = tab[2 * C + c + k];
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) r[j][k] = act_residual(r[j][k], mean, sc, sh);
+            __syncthreads();  // thread 0's acquire orders the partial reads below
+            for (int c = tid; c < C; c += T) {
+                const int g = c / cpg;
+                Welford acc{0.f, 0.f, 0.f};
+                for (int p = 0; p < P; ++p) {
+                    float4 q;
+                    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
+                                 : "l"(a.partials + (n * G + g) * P + p)
+                                 : "memory");
+                    acc = wf_merge(acc, Welford{q.x, q.y, q.z});
+                }
+                const float rstd = 1.f / sqrtf(acc.m2 / acc.n + a.eps);
+                tab[c] = make_float4(acc.mean, rstd * a.gamma[c] * (2.f * kLog2e), a.beta[c] * (2.f * kLog2e), 0.f);
             }
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) ms_fold<CH>(st[j], r[j]);
-        }
-        for (; c < C; ++c) {
-            const float* p = yp + (int64_t)c * HW;
-            float r[VEC][1];
-            if constexpr (VEC == 4) {
-                float4 a = ld_stream_f4(p);
-                r[0][0] = a.x; r[1][0] = a.y; r[2][0] = a.z; r[3][0] = a.w;
-            } else {
-                r[0][0] = ld_stream_f1(p);
-            }
-            const float mean = tab[c], sc = tab[C + c], sh = tab[2 * C + c];
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                r[j][0] = act_residual(r[j][0], mean, sc, sh);
-                ms_fold<1>(st[j], r[j]);
-            }
-        }
-        float* dst = out + n * HW + p0;
-        if constexpr (VEC == 4) {
-            *reinterpret_cast<float4*>(dst) =
-                make_float4(ms_lse(st[0]), ms_lse(st[1]), ms_lse(st[2]), ms_lse(st[3]));
-        } else {
-            dst[0] = ms_lse(st[0]);
+            __syncthreads();
+            const int64_t p0 = (idx * T + tid) * VEC;
+            if (p0 < HW)
+                apply_pixels<VEC, true>(a.y + n * (int64_t)C * HW + p0, tab, C, HW, a.out + n * HW + p0, drop);
         }
     }
 }
@@ -240,7 +408,7 @@ cudaError_t launch_gn_act_lse(const DeviceInfo& dev, const float* y, const float
         const int64_t nblk = N * tiles;
         const int64_t cap = (int64_t)dev.sm_count * 16 * 16;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nblk, cap));
-        const size_t smem = (size_t)3 * C * sizeof(float);
+        const size_t smem = (size_t)C * sizeof(float4);
         cudaError_t e;
         if (vec_apply) {
             if (smem > 48 * 1024) {
@@ -259,6 +427,74 @@ cudaError_t launch_gn_act_lse(const DeviceInfo& dev, const float* y, const float
         }
         return cudaGetLastError();
     }
+}
+
+static int gn_parts() { return std::max(1, std::min(16, env_int("LSE_GN_PARTS", 2))); }
+
+size_t gn_fused_scratch_bytes(int64_t N, int64_t G) {
+    return (size_t)N * G * gn_parts() * sizeof(float4) + ((size_t)N * sizeof(unsigned) + 15) / 16 * 16 + 16;
+}
+
+template <int VEC>
+static cudaError_t gn_fused_go(const DeviceInfo& dev, const GnFusedArgs& args, size_t smem, cudaStream_t stream) {
+    auto kern = gn_fused_kernel<VEC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    const int want = env_int("LSE_GN_CTAS_PER_SM", 0);
+    if (want > 0) per_sm = std::min(per_sm, want);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the sample waits end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    const int64_t items = args.N * ((int64_t)args.G * args.parts + args.tiles);
+    cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)per_sm * dev.sm_count)));
+    if (env_int("LSE_VERBOSE", 0))
+        fprintf(stderr, "[lse] gn_fused: grid=%u parts=%d tiles=%d lag=%d\n", cfg.gridDim.x, args.parts,
+                args.tiles, args.lag);
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const float* gamma,
+                                    const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
+                                    int64_t G, float eps, void* scratch, cudaStream_t stream) {
+    const bool vec = (HW % 4 == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
+    const int VEC = vec ? 4 : 1;
+    GnFusedArgs args;
+    args.y = y;
+    args.gamma = gamma;
+    args.beta = beta;
+    args.out = out;
+    args.N = N;
+    args.HW = HW;
+    args.C = (int)C;
+    args.G = (int)G;
+    args.parts = gn_parts();
+    args.tiles = (int)((HW + 256 * VEC - 1) / (256 * VEC));
+    args.lag = (int)std::min<int64_t>(N, std::max(0, env_int("LSE_GN_LAG", 8)));
+    args.eps = eps;
+    char* sp = static_cast<char*>(scratch);
+    args.partials = reinterpret_cast<float4*>(sp);
+    sp += (size_t)N * G * args.parts * sizeof(float4);
+    args.done = reinterpret_cast<unsigned*>(sp);
+    const size_t done_bytes = ((size_t)N * sizeof(unsigned) + 15) / 16 * 16;
+    args.next = reinterpret_cast<unsigned long long*>(sp + done_bytes);
+    args.status = dev.status;
+    cudaError_t e = cudaMemsetAsync(args.done, 0, done_bytes + 16, stream);
+    if (e != cudaSuccess) return e;
+    const size_t smem = (size_t)C * sizeof(float4);
+    return vec ? gn_fused_go<4>(dev, args, smem, stream) : gn_fused_go<1>(dev, args, smem, stream);
 }
 
 }  // namespace lse

@@ -71,6 +71,14 @@ cudaError_t launch_gn_act_lse(const DeviceInfo& dev, const float* y, const float
                               const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
                               int64_t G, float eps, float* stats, cudaStream_t stream);
 
+// Form 3 in one cooperative kernel: statistics parts and apply tiles of the
+// samples claimed from one work queue, each sample's second read close behind
+// its first so that it hits L2.  Scratch: gn_fused_scratch_bytes(N, G).
+size_t gn_fused_scratch_bytes(int64_t N, int64_t G);
+cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const float* gamma,
+                                    const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
+                                    int64_t G, float eps, void* scratch, cudaStream_t stream);
+
 // Largest C that the apply kernel's shared-memory table holds.
 constexpr int64_t kGnMaxChannels = 8192;
 

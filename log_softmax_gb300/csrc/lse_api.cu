@@ -188,11 +188,18 @@ lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, f
     if (st != LSE_OK) return st;
     cudaMemPool_t pool = nullptr;
     if ((st = device_pool(s, &pool)) != LSE_OK) return st;
+    // LSE_GN_VARIANT=1 selects the two-kernel path (statistics, then apply);
+    // the default is the one-kernel chain that re-reads each sample from L2.
+    const bool fused = env_int("LSE_GN_VARIANT", 0) != 1;
+    const size_t bytes = fused ? gn_fused_scratch_bytes(N, G) : (size_t)ng * 2 * sizeof(float);
     void* stats = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&stats, (size_t)ng * 2 * sizeof(float), pool, stream);
+    cudaError_t e = cudaMallocFromPoolAsync(&stats, bytes, pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    e = launch_gn_act_lse(s->info, y, gamma, beta, out, N, C, HW, G, eps, static_cast<float*>(stats),
-                          stream);
+    if (fused)
+        e = launch_gn_act_lse_fused(s->info, y, gamma, beta, out, N, C, HW, G, eps, stats, stream);
+    else
+        e = launch_gn_act_lse(s->info, y, gamma, beta, out, N, C, HW, G, eps, static_cast<float*>(stats),
+                              stream);
     cudaError_t ef = cudaFreeAsync(stats, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     if (ef != cudaSuccess) return cuda_fail(ef);

@@ -274,6 +274,27 @@ def test_gn_act_lse_parity(lib, N, C, H, W, G):
     assert_parity(got, ref, f"gn {N,C,H,W,G}")
 
 
+GN_CONFIGS = [
+    {"LSE_GN_VARIANT": "1"},                                    # statistics kernel + apply kernel
+    {"LSE_GN_VARIANT": "0"},                                    # one kernel, default parts / lag
+    {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "1", "LSE_GN_LAG": "0"},
+    {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "7", "LSE_GN_LAG": "2"},
+    {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "16", "LSE_GN_LAG": "100", "LSE_GN_CTAS_PER_SM": "1"},
+]
+
+
+@pytest.mark.parametrize("cfg", GN_CONFIGS,
+                         ids=["-".join(f"{k[7:]}{v}" for k, v in c.items()) for c in GN_CONFIGS])
+@pytest.mark.parametrize("N,C,H,W,G", [(5, 64, 20, 20, 16), (3, 8, 5, 7, 4), (2, 6, 1, 1, 3)])
+def test_gn_act_lse_variants(lib, env, cfg, N, C, H, W, G):
+    for k, v in cfg.items():
+        env.setenv(k, v)
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))
+    got = lib.gn_act_lse_forward(inp["y"].to(DEV), inp["gamma"].to(DEV), inp["beta"].to(DEV), G, 1e-5)
+    ref = oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], G, 1e-5)
+    assert_parity(got, ref, f"gn {cfg} {N,C,H,W,G}")
+
+
 def test_gn_act_lse_wide_range(lib):
     """Large gamma and shifted data: z spans about [-60, 60] (tanh saturates),
     a non-zero mean exercises the statistics."""
