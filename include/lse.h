@@ -87,6 +87,22 @@ lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64
                                  cudaStream_t stream);
 
 /*
+ * log_softmax_lastdim_host — log_softmax_lastdim on HOST buffers: x and out are
+ * host pointers (page-locked memory lets the copies run asynchronously and
+ * overlap; pageable memory works, with staged copies).  Rows are processed in
+ * chunks of about 256 MB (LSE_HOST_CHUNK_MB) through three device staging
+ * buffers from the library's pool: the copy in of one chunk, the computation of
+ * the previous one and the copy out of the one before overlap, on two copy
+ * streams the library owns, ordered after the work already queued on `stream`.
+ * `stream` resumes after the last copy out, so out is complete once `stream`
+ * is; the host must keep both buffers alive and untouched until then.  Calls
+ * on one device enqueue one at a time.  Same argument rules as
+ * log_softmax_lastdim (sizes, 4-byte alignment, NULL).
+ */
+lse_status_t log_softmax_lastdim_host(const float* x, float* out, int64_t rows, int64_t cols,
+                                      cudaStream_t stream);
+
+/*
  * gn_act_lse — GroupNorm -> tanh -> hardswish -> residual add -> logsumexp over
  * channels, keepdim ("Kimi-K2.6 / l2_p92", the chain after its Conv2d):
  *   mean[n,g], var[n,g] : population statistics of the C/G channels of group g

@@ -55,6 +55,8 @@ def load_library(path: str = LIB_PATH):
     i64, vp, f32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
     lib.lse_reduce.argtypes = [vp, vp, i64, i64, i64, vp]
     lib.log_softmax_lastdim.argtypes = [vp, vp, i64, i64, vp]
+    lib.log_softmax_lastdim_host.argtypes = [vp, vp, i64, i64, vp]
+    lib.log_softmax_lastdim_host.restype = ctypes.c_int
     lib.gn_act_lse.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
     lib.gn_act_lse_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
     lib.gn_act_lse_noalloc.restype = ctypes.c_int
@@ -130,6 +132,23 @@ def log_softmax_lastdim(x, out, rows: int, cols: int, stream=None) -> None:
     with _device_of(x):
         rc = lib.log_softmax_lastdim(_ptr(x), _ptr(out), int(rows), int(cols), _stream(stream, x))
     _check("log_softmax_lastdim", rc)
+
+
+def _host_ptr(t):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError("expected a CPU tensor")
+    if t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError("tensor must be contiguous float32")
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def log_softmax_lastdim_host(x, out, rows: int, cols: int, stream=None) -> None:
+    """log_softmax_lastdim on host (CPU) tensors, pipelined through the device; `out`
+    is complete once `stream` (default: the current stream) is."""
+    lib = load_library()
+    rc = lib.log_softmax_lastdim_host(_host_ptr(x), _host_ptr(out), int(rows), int(cols),
+                                      _stream(stream))
+    _check("log_softmax_lastdim_host", rc)
 
 
 def gn_act_lse(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: float,
@@ -228,6 +247,18 @@ def logsumexp(x: torch.Tensor, dim: int = 0, keepdim: bool = False, out=None,
 def log_softmax(x: torch.Tensor, out=None, device="cuda") -> torch.Tensor:
     """log_softmax over the last axis of fp32 x (any leading shape).  CPU input is copied
     to `device` and the result back to host memory (`out` if given)."""
+    if not x.is_cuda:
+        # host in, host out: the library pipelines chunks through the device
+        xh = x.contiguous()
+        cols = xh.shape[-1] if xh.ndim else 1
+        rows = xh.numel() // cols if cols else 0
+        oh = out if out is not None else torch.empty(xh.shape, dtype=torch.float32,
+                                                     pin_memory=xh.is_pinned())
+        with torch.cuda.device(torch.device(device)):
+            stream = torch.cuda.current_stream()
+            log_softmax_lastdim_host(xh, oh, rows, cols, stream=stream)
+            stream.synchronize()
+        return oh
     xd, host = _to_device(x, device)
     cols = xd.shape[-1] if xd.ndim else 1
     rows = xd.numel() // cols if cols else 0

@@ -1,5 +1,6 @@
 // C ABI of liblse.so: argument checks, variant choice, scratch, status.
 // Declarations and the contract of each entry point are in include/lse.h.
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -14,10 +15,21 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Copy streams and events of the host-buffer pipeline (created on first use).
+constexpr int kHostBufs = 3;
+struct HostPipe {
+    bool ready = false;
+    std::mutex mu;  // one pipeline enqueue at a time per device
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t ev_h2d[kHostBufs] = {}, ev_comp[kHostBufs] = {}, ev_d2h[kHostBufs] = {};
+};
+
 struct DeviceState {
     bool ready = false;
     DeviceInfo info;
     cudaMemPool_t pool = nullptr;
+    HostPipe pipe;
 };
 
 std::mutex g_mu;
@@ -78,6 +90,27 @@ lse_status_t device_pool(DeviceState* s, cudaMemPool_t* pool) {
         if (e != cudaSuccess) return cuda_fail(e);
     }
     *pool = s->pool;
+    return LSE_OK;
+}
+
+lse_status_t host_pipe(DeviceState* s, HostPipe** out) {
+    HostPipe& hp = s->pipe;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!hp.ready) {
+        cudaError_t e;
+        if ((e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e);
+        for (int b = 0; b < kHostBufs; ++b) {
+            if ((e = cudaEventCreateWithFlags(&hp.ev_h2d[b], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.ev_comp[b], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.ev_d2h[b], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e);
+        }
+        hp.ready = true;
+    }
+    *out = &hp;
     return LSE_OK;
 }
 
@@ -203,6 +236,72 @@ lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, f
     cudaError_t ef = cudaFreeAsync(stats, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     if (ef != cudaSuccess) return cuda_fail(ef);
+    return LSE_OK;
+}
+
+lse_status_t log_softmax_lastdim_host(const float* x, float* out, int64_t rows, int64_t cols,
+                                      cudaStream_t stream) {
+    if (rows < 0 || cols < 0) return LSE_ERR_SIZE;
+    int64_t n = 0;
+    if (!mul_ok(rows, cols, &n) || n > INT64_MAX / 4) return LSE_ERR_SIZE;
+    if (n == 0) return LSE_OK;
+    if (!x || !out) return LSE_ERR_NULL;
+    if (!aligned4(x) || !aligned4(out)) return LSE_ERR_ALIGN;
+    DeviceState* s = nullptr;
+    lse_status_t st = device_state(&s);
+    if (st != LSE_OK) return st;
+    cudaMemPool_t pool = nullptr;
+    if ((st = device_pool(s, &pool)) != LSE_OK) return st;
+    HostPipe* hp = nullptr;
+    if ((st = host_pipe(s, &hp)) != LSE_OK) return st;
+
+    // Chunks of whole rows of about LSE_HOST_CHUNK_MB (default 256) MB each,
+    // three in flight: the copy in of chunk i+1, the call on chunk i and the
+    // copy out of chunk i-1 overlap.
+    const int64_t row_bytes = cols * 4;
+    const int64_t target = (int64_t)std::max(1, env_int("LSE_HOST_CHUNK_MB", 256)) << 20;
+    const int64_t chunk_rows = std::max<int64_t>(1, std::min<int64_t>(rows, target / row_bytes));
+    const int64_t nchunks = (rows + chunk_rows - 1) / chunk_rows;
+    const size_t buf_bytes = (size_t)((chunk_rows * row_bytes + 255) / 256 * 256);
+
+    std::lock_guard<std::mutex> lock(hp->mu);
+    void* mem = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&mem, 2 * kHostBufs * buf_bytes, pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    auto din = [&](int b) { return reinterpret_cast<float*>(static_cast<char*>(mem) + (size_t)b * buf_bytes); };
+    auto dout = [&](int b) {
+        return reinterpret_cast<float*>(static_cast<char*>(mem) + (size_t)(kHostBufs + b) * buf_bytes);
+    };
+    // Order the copy streams after everything already queued on `stream`
+    // (including the staging allocation).
+    if ((e = cudaEventRecord(hp->start, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->h2d, hp->start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->d2h, hp->start, 0)) != cudaSuccess)
+        return cuda_fail(e);
+    for (int64_t i = 0; i < nchunks; ++i) {
+        const int b = (int)(i % kHostBufs);
+        const int64_t r0 = i * chunk_rows;
+        const int64_t nr = std::min(chunk_rows, rows - r0);
+        const size_t bytes = (size_t)(nr * row_bytes);
+        // buffer b is free once chunk i - kHostBufs has been copied out
+        if (i >= kHostBufs && (e = cudaStreamWaitEvent(hp->h2d, hp->ev_d2h[b], 0)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(din(b), x + r0 * cols, bytes, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
+            (e = cudaEventRecord(hp->ev_h2d[b], hp->h2d)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(stream, hp->ev_h2d[b], 0)) != cudaSuccess)
+            return cuda_fail(e);
+        st = log_softmax_lastdim(din(b), dout(b), nr, cols, stream);
+        if (st != LSE_OK) return st;
+        if ((e = cudaEventRecord(hp->ev_comp[b], stream)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hp->d2h, hp->ev_comp[b], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(out + r0 * cols, dout(b), bytes, cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess ||
+            (e = cudaEventRecord(hp->ev_d2h[b], hp->d2h)) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    // `stream` resumes after the last copy out; then the staging memory returns.
+    for (int b = 0; b < kHostBufs && b < nchunks; ++b)
+        if ((e = cudaStreamWaitEvent(stream, hp->ev_d2h[b], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaFreeAsync(mem, stream)) != cudaSuccess) return cuda_fail(e);
     return LSE_OK;
 }
 

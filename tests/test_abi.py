@@ -80,6 +80,7 @@ LSM_ERRORS = [
 @pytest.mark.parametrize("args,want", LSM_ERRORS)
 def test_log_softmax_validation(lib, args, want):
     assert lib.log_softmax_lastdim(*args, None) == want
+    assert lib.log_softmax_lastdim_host(*args, None) == want
 
 
 GN_ERRORS = [

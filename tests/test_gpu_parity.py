@@ -357,3 +357,27 @@ def test_log_softmax_persistent_long_rows(lib):
     its shared-memory slice while writing the previous row."""
     x = synth.normal((64, 393216), seed=12)
     assert_parity(_log_softmax(lib, x), oracle.log_softmax(x), "64 x 393216")
+
+
+@pytest.mark.parametrize("rows,cols,chunk_mb,pinned", [
+    (37, 100000, "1", True),      # many chunks, last one short
+    (5, 393216, "1", False),      # pageable buffers, one row per chunk
+    (300, 4099, "", True),        # one chunk, unaligned rows
+    (9, 65536, "2", True),
+])
+def test_log_softmax_host_pipeline(lib, env, rows, cols, chunk_mb, pinned):
+    """Host buffers in and out, pipelined through device staging buffers."""
+    env.setenv("LSE_HOST_CHUNK_MB", chunk_mb)
+    x = synth.normal((rows, cols), seed=rows + cols)
+    if pinned:
+        x = x.pin_memory()
+    out = torch.full((rows, cols), float("nan"))
+    if pinned:
+        out = out.pin_memory()
+    s = torch.cuda.current_stream()
+    lib.log_softmax_lastdim_host(x, out, rows, cols, stream=s)
+    s.synchronize()
+    assert_parity(out, oracle.log_softmax(x), f"host pipeline {rows}x{cols}")
+    got = lib.log_softmax(x)   # the convenience routes host tensors through the same entry
+    assert not got.is_cuda
+    assert_parity(got, oracle.log_softmax(x), "host convenience")
