@@ -243,16 +243,18 @@ __device__ __forceinline__ Welford block_welford(const float* __restrict__ base,
     const int64_t nv = (hi - lo) / VEC;
     const float* b = base + lo;
     int64_t i = tid;
-    for (; i + 3 * T < nv; i += 4 * T) {
-        float v[4 * VEC];
+    // UNR loads in flight per thread (8 x 16 B), then one exact batch Welford
+    constexpr int UNR = 8;
+    for (; i + (UNR - 1) * T < nv; i += UNR * T) {
+        float v[UNR * VEC];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < UNR; ++k) {
             float q[VEC];
             load_vec<VEC, true>(b + (i + k * T) * VEC, q, policy);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) v[k * VEC + e] = q[e];
         }
-        w = wf_merge(w, wf_batch<4 * VEC>(v));
+        w = wf_merge(w, wf_batch<UNR * VEC>(v));
     }
     for (; i < nv; i += T) {
         float q[VEC];
@@ -291,9 +293,8 @@ struct GnFusedArgs {
 // (the grid is cooperative: all CTAs resident) and wait on nothing, so the wait
 // ends.  The lag keeps each sample's second read close behind its first, while
 // the sample (4 MB at 64 x 126 x 126) is still in L2: HBM sees y once.
-template <int VEC>
-__global__ void __launch_bounds__(256) gn_fused_kernel(const GnFusedArgs a) {
-    constexpr int T = 256;
+template <int VEC, int T>
+__global__ void __launch_bounds__(T) gn_fused_kernel(const GnFusedArgs a) {
     extern __shared__ float4 tab[];  // [C] {mean, rstd*gamma*2log2e, beta*2log2e, 0}
     __shared__ Welford red[32];
     __shared__ long long item_sh;
@@ -429,19 +430,19 @@ cudaError_t launch_gn_act_lse(const DeviceInfo& dev, const float* y, const float
     }
 }
 
-static int gn_parts() { return std::max(1, std::min(16, env_int("LSE_GN_PARTS", 2))); }
+static int gn_parts() { return std::max(1, std::min(16, env_int("LSE_GN_PARTS", 1))); }
 
 size_t gn_fused_scratch_bytes(int64_t N, int64_t G) {
     return (size_t)N * G * gn_parts() * sizeof(float4) + ((size_t)N * sizeof(unsigned) + 15) / 16 * 16 + 16;
 }
 
-template <int VEC>
+template <int VEC, int T>
 static cudaError_t gn_fused_go(const DeviceInfo& dev, const GnFusedArgs& args, size_t smem, cudaStream_t stream) {
-    auto kern = gn_fused_kernel<VEC>;
+    auto kern = gn_fused_kernel<VEC, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
     const int want = env_int("LSE_GN_CTAS_PER_SM", 0);
@@ -452,14 +453,14 @@ static cudaError_t gn_fused_go(const DeviceInfo& dev, const GnFusedArgs& args, s
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(T);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     const int64_t items = args.N * ((int64_t)args.G * args.parts + args.tiles);
     cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)per_sm * dev.sm_count)));
     if (env_int("LSE_VERBOSE", 0))
-        fprintf(stderr, "[lse] gn_fused: grid=%u parts=%d tiles=%d lag=%d\n", cfg.gridDim.x, args.parts,
-                args.tiles, args.lag);
+        fprintf(stderr, "[lse] gn_fused: grid=%u threads=%d parts=%d tiles=%d lag=%d\n", cfg.gridDim.x, T,
+                args.parts, args.tiles, args.lag);
     e = cudaLaunchKernelEx(&cfg, kern, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -481,8 +482,9 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     args.C = (int)C;
     args.G = (int)G;
     args.parts = gn_parts();
-    args.tiles = (int)((HW + 256 * VEC - 1) / (256 * VEC));
-    args.lag = (int)std::min<int64_t>(N, std::max(0, env_int("LSE_GN_LAG", 8)));
+    const int T = env_int("LSE_GN_THREADS", 256);
+    args.tiles = (int)((HW + (int64_t)T * VEC - 1) / ((int64_t)T * VEC));
+    args.lag = (int)std::min<int64_t>(N, std::max(0, env_int("LSE_GN_LAG", 16)));
     args.eps = eps;
     char* sp = static_cast<char*>(scratch);
     args.partials = reinterpret_cast<float4*>(sp);
@@ -494,7 +496,9 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     cudaError_t e = cudaMemsetAsync(args.done, 0, done_bytes + 16, stream);
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)C * sizeof(float4);
-    return vec ? gn_fused_go<4>(dev, args, smem, stream) : gn_fused_go<1>(dev, args, smem, stream);
+    if (T == 1024) return vec ? gn_fused_go<4, 1024>(dev, args, smem, stream) : gn_fused_go<1, 1024>(dev, args, smem, stream);
+    if (T == 512) return vec ? gn_fused_go<4, 512>(dev, args, smem, stream) : gn_fused_go<1, 512>(dev, args, smem, stream);
+    return vec ? gn_fused_go<4, 256>(dev, args, smem, stream) : gn_fused_go<1, 256>(dev, args, smem, stream);
 }
 
 }  // namespace lse

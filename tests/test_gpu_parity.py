@@ -280,6 +280,8 @@ GN_CONFIGS = [
     {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "1", "LSE_GN_LAG": "0"},
     {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "7", "LSE_GN_LAG": "2"},
     {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "16", "LSE_GN_LAG": "100", "LSE_GN_CTAS_PER_SM": "1"},
+    {"LSE_GN_VARIANT": "0", "LSE_GN_THREADS": "512", "LSE_GN_LAG": "3"},
+    {"LSE_GN_VARIANT": "0", "LSE_GN_THREADS": "1024", "LSE_GN_PARTS": "3"},
 ]
 
 
