@@ -64,8 +64,13 @@ class Oracle:
         lib.oracle_row_lse.argtypes = [vp, vp, i64, i64]
         lib.oracle_gn_act_lse.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64,
                                           ctypes.c_double, vp, vp]
+        lib.oracle_softmax.argtypes = [vp, vp, i64, i64]
+        lib.oracle_log_softmax_dim.argtypes = [vp, vp, i64, i64, i64]
+        for name in ("oracle_group_norm", "oracle_gn_act_residual"):
+            getattr(lib, name).argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_double]
         for f in (lib.oracle_lse_reduce, lib.oracle_log_softmax, lib.oracle_row_lse,
-                  lib.oracle_gn_act_lse):
+                  lib.oracle_gn_act_lse, lib.oracle_softmax, lib.oracle_log_softmax_dim,
+                  lib.oracle_group_norm, lib.oracle_gn_act_residual):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -133,6 +138,47 @@ class Oracle:
         return out
 
 
+    def softmax(self, x) -> np.ndarray:
+        """softmax over the last axis of a 2-d (rows, cols) array."""
+        x = _f32(x)
+        rows, cols = x.shape
+        out = np.empty((rows, cols), dtype=np.float64)
+        rc = self.lib.oracle_softmax(_p(x), _p(out), rows, cols)
+        if rc != 0:
+            raise ValueError(f"oracle_softmax rejected its arguments (rc={rc})")
+        return out
+
+    def log_softmax_dim(self, x, outer: int, R: int, inner: int) -> np.ndarray:
+        """log_softmax over the middle axis of x viewed as (outer, R, inner)."""
+        x = _f32(x)
+        assert x.size == outer * R * inner
+        out = np.empty((outer, R, inner), dtype=np.float64)
+        rc = self.lib.oracle_log_softmax_dim(_p(x), _p(out), outer, R, inner)
+        if rc != 0:
+            raise ValueError(f"oracle_log_softmax_dim rejected its arguments (rc={rc})")
+        return out
+
+    def _gn_elementwise(self, fn, y, gamma, beta, G, eps):
+        y = _f32(y)
+        gamma = _f32(gamma)
+        beta = _f32(beta)
+        N, C = y.shape[0], y.shape[1]
+        HW = int(np.prod(y.shape[2:])) if y.ndim > 2 else 1
+        out = np.empty(y.shape, dtype=np.float64)
+        rc = fn(_p(y), _p(gamma), _p(beta), _p(out), N, C, HW, G, float(np.float32(eps)))
+        if rc != 0:
+            raise ValueError(f"oracle rejected its arguments (rc={rc})")
+        return out
+
+    def group_norm(self, y, gamma, beta, G: int, eps: float = 1e-5) -> np.ndarray:
+        """GroupNorm with per-channel affine, y of shape (N, C, *spatial)."""
+        return self._gn_elementwise(self.lib.oracle_group_norm, y, gamma, beta, G, eps)
+
+    def gn_act_residual(self, y, gamma, beta, G: int, eps: float = 1e-5) -> np.ndarray:
+        """y + hardswish(tanh(GroupNorm(y))), y of shape (N, C, *spatial)."""
+        return self._gn_elementwise(self.lib.oracle_gn_act_residual, y, gamma, beta, G, eps)
+
+
 def default() -> Oracle:
     """The committed oracle, compiled on first use."""
     global _default
@@ -160,3 +206,19 @@ def row_lse(x) -> np.ndarray:
 
 def gn_act_lse(y, gamma, beta, G: int, eps: float = 1e-5, return_stats: bool = False):
     return default().gn_act_lse(y, gamma, beta, G, eps, return_stats)
+
+
+def softmax(x) -> np.ndarray:
+    return default().softmax(x)
+
+
+def log_softmax_dim(x, outer: int, R: int, inner: int) -> np.ndarray:
+    return default().log_softmax_dim(x, outer, R, inner)
+
+
+def group_norm(y, gamma, beta, G: int, eps: float = 1e-5) -> np.ndarray:
+    return default().group_norm(y, gamma, beta, G, eps)
+
+
+def gn_act_residual(y, gamma, beta, G: int, eps: float = 1e-5) -> np.ndarray:
+    return default().gn_act_residual(y, gamma, beta, G, eps)

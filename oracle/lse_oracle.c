@@ -174,3 +174,74 @@ int oracle_gn_act_lse(const float* y, const float* gamma, const float* beta, dou
     free(r);
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Neighbouring operations of the same method.
+ * ------------------------------------------------------------------------ */
+
+/* Softmax of each row ([P2] describes it beside LogSoftmax as exp(x - m)
+ * scaled by 1 / sum): out[row, j] = exp(x[row, j] - lse(row)). */
+int oracle_softmax(const float* x, double* out, int64_t rows, int64_t cols)
+{
+    if (!x || !out || rows < 0 || cols <= 0) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* row = x + r * cols;
+        double lse = lse_strided_float(row, cols, 1);
+        for (int64_t j = 0; j < cols; ++j) out[r * cols + j] = exp((double)row[j] - lse);
+    }
+    return 0;
+}
+
+/* LogSoftmax along the middle axis of a contiguous (outer, R, inner) tensor:
+ * out[o, r, i] = x[o, r, i] - lse over r' of x[o, r', i]. */
+int oracle_log_softmax_dim(const float* x, double* out, int64_t outer, int64_t R, int64_t inner)
+{
+    if (!x || !out || outer < 0 || R <= 0 || inner < 0) return -1;
+    for (int64_t o = 0; o < outer; ++o)
+        for (int64_t i = 0; i < inner; ++i) {
+            const float* col = x + o * R * inner + i;
+            double lse = lse_strided_float(col, R, inner);
+            for (int64_t r = 0; r < R; ++r)
+                out[(o * R + r) * inner + i] = (double)col[r * inner] - lse;
+        }
+    return 0;
+}
+
+/* [P3] GroupNorm alone (act = 0): out = (y - mean_g) / sqrt(var_g + eps) * gamma_c + beta_c,
+ * or the chain without the channel reduction (act = 1):
+ * out = y + hardswish(tanh(GroupNorm(y))).  y, out are [N, C, HW]. */
+static int group_norm_impl(const float* y, const float* gamma, const float* beta, double* out,
+                           int64_t N, int64_t C, int64_t HW, int64_t G, double eps, int act)
+{
+    if (!y || !gamma || !beta || !out || N < 0 || C <= 0 || HW < 0 || G <= 0 || C % G != 0)
+        return -1;
+    const int64_t cpg = C / G;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < G; ++g) {
+            const float* span = y + (n * C + g * cpg) * HW;
+            double mu, var;
+            group_stats(span, cpg * HW, &mu, &var);
+            double rs = 1.0 / sqrt(var + eps);
+            for (int64_t cc = 0; cc < cpg; ++cc) {
+                int64_t c = g * cpg + cc;
+                for (int64_t p = 0; p < HW; ++p) {
+                    double v = (double)y[(n * C + c) * HW + p];
+                    double z = (v - mu) * rs * (double)gamma[c] + (double)beta[c];
+                    out[(n * C + c) * HW + p] = act ? v + hardswish(tanh(z)) : z;
+                }
+            }
+        }
+    return 0;
+}
+
+int oracle_group_norm(const float* y, const float* gamma, const float* beta, double* out,
+                      int64_t N, int64_t C, int64_t HW, int64_t G, double eps)
+{
+    return group_norm_impl(y, gamma, beta, out, N, C, HW, G, eps, 0);
+}
+
+int oracle_gn_act_residual(const float* y, const float* gamma, const float* beta, double* out,
+                           int64_t N, int64_t C, int64_t HW, int64_t G, double eps)
+{
+    return group_norm_impl(y, gamma, beta, out, N, C, HW, G, eps, 1);
+}

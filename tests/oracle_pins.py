@@ -250,6 +250,102 @@ def pin_gn_single_channel(orc):
         _close(out.reshape(-1), [want], atol=1e-14)
 
 
+# --------------------------------------------------------------------- softmax, other axes, GroupNorm alone
+
+def pin_softmax_normalised(orc):
+    """rows sum to 1 and out_j / out_k = exp(x_j - x_k); a constant row gives 1/cols."""
+    rng = _rng(41)
+    x = rng.normal(0, 3, size=(5, 77)).astype(np.float32)
+    out = orc.softmax(x)
+    _close(out.sum(axis=1), np.ones(5), atol=1e-13)
+    _close(out / out[:, :1], np.exp(x.astype(np.float64) - x[:, :1].astype(np.float64)),
+           rtol=1e-12, atol=0)
+    _close(orc.softmax(np.full((2, 6), 4.5, np.float32)), np.full((2, 6), 1 / 6), atol=1e-15)
+
+
+def pin_softmax_torch(orc):
+    """agrees with torch.softmax in float64, with -inf entries and an all -inf row."""
+    rng = _rng(42)
+    x = rng.normal(0, 2, size=(5, 300)).astype(np.float32)
+    x[rng.random(size=x.shape) < 0.02] = -np.inf
+    x[4, :] = -np.inf
+    ref = torch.softmax(torch.from_numpy(x).double(), dim=1).numpy()
+    out = orc.softmax(x)
+    assert np.array_equal(np.isnan(out), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    _close(out[fin], ref[fin], atol=1e-14)
+
+
+def pin_softmax_special(orc):
+    """softmax = exp(log_softmax): a row holding +inf gives NaN at the +inf and 0 elsewhere
+    (torch's (x - max) / sum gives NaN throughout; the reading follows log_softmax); a NaN
+    row gives NaN; -inf entries give exactly 0."""
+    inf, nan = float("inf"), float("nan")
+    x = np.array([[1.0, inf, 2.0], [1.0, nan, 2.0], [0.0, -inf, 0.0]], dtype=np.float32)
+    out = orc.softmax(x)
+    assert math.isnan(out[0, 1]) and out[0, 0] == 0.0 and out[0, 2] == 0.0
+    assert np.isnan(out[1]).all()
+    assert out[2, 1] == 0.0
+    _close(out[2, [0, 2]], [0.5, 0.5], atol=1e-15)
+
+
+def pin_log_softmax_dim_torch(orc):
+    """log_softmax over the middle axis agrees with torch.log_softmax(dim=1) in float64."""
+    rng = _rng(43)
+    for outer, R, inner in ((2, 5, 7), (1, 33, 3), (3, 4, 1), (2, 1, 5)):
+        x = rng.normal(0, 4, size=(outer, R, inner)).astype(np.float32)
+        ref = torch.log_softmax(torch.from_numpy(x).double(), dim=1).numpy()
+        _close(orc.log_softmax_dim(x, outer, R, inner), ref, atol=1e-13)
+
+
+def pin_log_softmax_dim_bruteforce(orc):
+    """each output x[o,r,i] - ln(sum over r' of exp x[o,r',i]) in 60-digit decimal."""
+    rng = _rng(44)
+    x = rng.uniform(-25, 25, size=(2, 3, 4)).astype(np.float32)
+    out = orc.log_softmax_dim(x, 2, 3, 4)
+    ref = np.array([[[float(x[o, r, i]) - _dec_lse(x[o, :, i]) for i in range(4)] for r in range(3)]
+                    for o in range(2)])
+    _close(out, ref, rtol=1e-14, atol=1e-13)
+
+
+def pin_group_norm_torch(orc):
+    """GroupNorm alone agrees with torch.nn.functional.group_norm in float64."""
+    rng = _rng(45)
+    for (N, C, H, W, G) in ((2, 8, 3, 5, 4), (1, 6, 2, 2, 3), (2, 4, 1, 7, 1), (1, 16, 4, 4, 16)):
+        y = rng.normal(1.5, 2.0, size=(N, C, H, W)).astype(np.float32)
+        gamma = rng.uniform(0.5, 1.5, size=C).astype(np.float32)
+        beta = rng.normal(0, 0.3, size=C).astype(np.float32)
+        ref = F.group_norm(torch.from_numpy(y).double(), G, torch.from_numpy(gamma).double(),
+                           torch.from_numpy(beta).double(), eps=float(np.float32(1e-5))).numpy()
+        _close(orc.group_norm(y, gamma, beta, G, 1e-5), ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_group_norm_moments(orc):
+    """with gamma = 1, beta = 0 every group of the output has mean 0 and population variance
+    var / (var + eps), var from numpy."""
+    rng = _rng(46)
+    N, C, HW, G, eps = 2, 6, 9, 3, 0.5
+    y = rng.normal(3, 1.5, size=(N, C, HW)).astype(np.float32)
+    out = orc.group_norm(y, np.ones(C, np.float32), np.zeros(C, np.float32), G, eps).reshape(N, G, -1)
+    var = y.astype(np.float64).reshape(N, G, -1).var(axis=2)
+    _close(out.mean(axis=2), np.zeros((N, G)), atol=1e-13)
+    _close(out.var(axis=2), var / (var + eps), rtol=1e-12)
+
+
+def pin_gn_act_residual_torch(orc):
+    """y + hardswish(tanh(GroupNorm(y))) agrees with the float64 torch composition."""
+    rng = _rng(47)
+    N, C, H, W, G = 2, 8, 3, 4, 2
+    y = rng.normal(0, 1, size=(N, C, H, W)).astype(np.float32)
+    gamma = rng.uniform(0.5, 1.5, size=C).astype(np.float32)
+    beta = rng.normal(0, 0.3, size=C).astype(np.float32)
+    y64 = torch.from_numpy(y).double()
+    z = F.group_norm(y64, G, torch.from_numpy(gamma).double(), torch.from_numpy(beta).double(),
+                     eps=float(np.float32(1e-5)))
+    ref = (y64 + F.hardswish(torch.tanh(z))).numpy()
+    _close(orc.gn_act_residual(y, gamma, beta, G, 1e-5), ref, rtol=1e-12, atol=1e-12)
+
+
 # --------------------------------------------------------------------- stored closed forms
 
 def pin_golden_closed_forms(orc):

@@ -37,6 +37,15 @@ MUTANTS = [
     ("channel_lse_drops_max", "return m + log(s);", "return log(s);", 0),
     ("mean_not_subtracted", "double d = (double)p[k] - mean;", "double d = (double)p[k];", 0),
     ("beta_dropped", " + (double)beta[c];", ";", 0),
+    ("softmax_without_exp", "out[r * cols + j] = exp((double)row[j] - lse);",
+     "out[r * cols + j] = (double)row[j] - lse;", 0),
+    ("softmax_unshifted", "exp((double)row[j] - lse)", "exp((double)row[j])", 0),
+    ("dim_softmax_stride", "lse_strided_float(col, R, inner)", "lse_strided_float(col, R, 1)", 0),
+    ("dim_softmax_index", "(double)col[r * inner] - lse", "(double)col[r] - lse", 0),
+    ("groupnorm_eps_dropped", "double rs = 1.0 / sqrt(var + eps);", "double rs = 1.0 / sqrt(var);", 0),
+    ("chain_no_residual", "act ? v + hardswish(tanh(z)) : z", "act ? hardswish(tanh(z)) : z", 0),
+    ("groupnorm_affine_swapped", "(v - mu) * rs * (double)gamma[c] + (double)beta[c]",
+     "(v - mu) * rs * (double)beta[c] + (double)gamma[c]", 0),
 ]
 
 
