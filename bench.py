@@ -48,19 +48,28 @@ def algorithmic_bytes(w: synth.Workload) -> int:
         R = w.shape[0]
         inner = w.numel // R
         return 4 * (w.numel + inner)
-    if w.op == "log_softmax":
+    if w.op in ("log_softmax", "softmax", "log_softmax_dim0"):
         return 4 * 2 * w.numel
     if w.op == "gn_act_lse":
         N, C, H, W = w.shape
         return 4 * (w.numel + 2 * C + N * H * W)
+    if w.op in GN_ELEMENTWISE:
+        C = w.shape[1]
+        return 4 * (2 * w.numel + 2 * C)
     raise KeyError(w.op)
 
+
+GN_ELEMENTWISE = ("group_norm", "gn_act_residual")
 
 # Kernels each step launches (the dominant kernel first).
 LAUNCHES = {
     "lse_dim0": ["lse_strided_kernel"],
     "log_softmax": ["lsm_ws_kernel"],
     "gn_act_lse": ["gn_fused_kernel"],
+    "softmax": ["lsm_ws_kernel"],
+    "log_softmax_dim0": ["lse_strided_kernel"],
+    "group_norm": ["gn_fused_kernel"],
+    "gn_act_residual": ["gn_fused_kernel"],
 }
 
 
@@ -70,25 +79,54 @@ def make_step(L, w: synth.Workload, inputs, out, stream):
         inner = w.numel // R
         x = inputs["x"]
         return lambda: L.lse_reduce(x, out, 1, R, inner, stream=stream)
-    if w.op == "log_softmax":
+    if w.op in ("log_softmax", "softmax"):
         rows, cols = w.shape
         x = inputs["x"]
-        return lambda: L.log_softmax_lastdim(x, out, rows, cols, stream=stream)
-    if w.op == "gn_act_lse":
+        fn = L.log_softmax_lastdim if w.op == "log_softmax" else L.softmax_lastdim
+        return lambda: fn(x, out, rows, cols, stream=stream)
+    if w.op == "log_softmax_dim0":
+        R = w.shape[0]
+        inner = w.numel // R
+        x = inputs["x"]
+        return lambda: L.log_softmax_dim(x, out, 1, R, inner, stream=stream)
+    if w.op == "gn_act_lse" or w.op in GN_ELEMENTWISE:
         N, C, H, W = w.shape
         y, g, b = inputs["y"], inputs["gamma"], inputs["beta"]
         G, eps = w.params["G"], w.params["eps"]
-        return lambda: L.gn_act_lse(y, g, b, out, N, C, H * W, G, eps, stream=stream)
+        fn = getattr(L, w.op)
+        return lambda: fn(y, g, b, out, N, C, H * W, G, eps, stream=stream)
     raise KeyError(w.op)
 
 
 def out_shape(w: synth.Workload):
     if w.op == "lse_dim0":
         return w.shape[1:]
-    if w.op == "log_softmax":
-        return w.shape
-    N, C, H, W = w.shape
-    return (N, 1, H, W)
+    if w.op == "gn_act_lse":
+        N, C, H, W = w.shape
+        return (N, 1, H, W)
+    return w.shape
+
+
+def oracle_call(w: synth.Workload, inputs) -> int:
+    """Runs the oracle on host inputs of the workload's kind (any size); returns
+    the algorithmic bytes of that call."""
+    import oracle
+    if w.op in ("log_softmax", "softmax"):
+        x = inputs["x"]
+        (oracle.log_softmax if w.op == "log_softmax" else oracle.softmax)(x)
+        return 8 * x.numel()
+    if w.op in ("lse_dim0", "log_softmax_dim0"):
+        x = inputs["x"].reshape(inputs["x"].shape[0], -1)
+        if w.op == "lse_dim0":
+            oracle.lse_reduce(x, 1, x.shape[0], x.shape[1])
+            return 4 * (x.numel() + x.shape[1])
+        oracle.log_softmax_dim(x, 1, x.shape[0], x.shape[1])
+        return 8 * x.numel()
+    y, g, b = inputs["y"], inputs["gamma"], inputs["beta"]
+    getattr(oracle, w.op)(y, g, b, w.params["G"], w.params["eps"])
+    if w.op == "gn_act_lse":
+        return 4 * (y.numel() + y.shape[0] * y.shape[2] * y.shape[3])
+    return 8 * y.numel()
 
 
 # ------------------------------------------------------------------ distributed
@@ -247,32 +285,27 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def time_oracle(w: synth.Workload, x_host, budget_s: float, unit_rows: int):
-    """Runs the oracle over successive slices of the sample, cycling through the
-    sample, until budget_s has passed.  Returns (bytes, seconds, slices done)."""
-    import oracle
-    n_units = {"log_softmax": lambda: x_host.shape[0] // unit_rows,
-               "lse_dim0": lambda: x_host.shape[1] // unit_rows,
-               "gn_act_lse": lambda: x_host[0].shape[0] // unit_rows}[w.op]()
+def time_oracle(w: synth.Workload, sample, budget_s: float, unit: int):
+    """Runs the oracle over successive slices of `unit` rows / columns / samples of
+    the host sample, cycling through it, until budget_s has passed.  Returns
+    (bytes, seconds, slices done)."""
+    if w.op in ("lse_dim0", "log_softmax_dim0"):
+        n_units = sample["x"].shape[1] // unit
+    else:
+        n_units = next(iter(sample.values())).shape[0] // unit
     n_units = max(1, n_units)
     t0 = time.perf_counter()
     done_bytes = 0
     units = 0
     while True:
         k = units % n_units
-        if w.op == "log_softmax":
-            sl = x_host[k * unit_rows:(k + 1) * unit_rows]
-            oracle.log_softmax(sl)
-            done_bytes += 8 * sl.numel()
-        elif w.op == "lse_dim0":
-            sl = x_host[:, k * unit_rows:(k + 1) * unit_rows].contiguous()
-            oracle.lse_reduce(sl, 1, sl.shape[0], sl.shape[1])
-            done_bytes += 4 * (sl.numel() + sl.shape[1])
+        if w.op in ("lse_dim0", "log_softmax_dim0"):
+            sl = {"x": sample["x"][:, k * unit:(k + 1) * unit].contiguous()}
+        elif "x" in sample:
+            sl = {"x": sample["x"][k * unit:(k + 1) * unit]}
         else:
-            y, g, b = x_host
-            sl = y[k * unit_rows:(k + 1) * unit_rows]
-            oracle.gn_act_lse(sl, g, b, w.params["G"], w.params["eps"])
-            done_bytes += 4 * (sl.numel() + sl.shape[0] * sl.shape[2] * sl.shape[3])
+            sl = dict(sample, y=sample["y"][k * unit:(k + 1) * unit])
+        done_bytes += oracle_call(w, sl)
         units += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -280,16 +313,27 @@ def time_oracle(w: synth.Workload, x_host, budget_s: float, unit_rows: int):
 
 
 def oracle_sample(w: synth.Workload, inputs_dev, rows: int):
-    """The first `rows` units (rows / columns / samples) of the workload on the host."""
-    if w.op == "log_softmax":
-        return inputs_dev["x"][:rows].cpu().contiguous(), 1
-    if w.op == "lse_dim0":
+    """The first `rows` units (rows / columns / samples) of the workload on the
+    host, and the slice size one oracle call takes."""
+    if w.op in ("log_softmax", "softmax"):
+        return {"x": inputs_dev["x"][:rows].cpu().contiguous()}, 1
+    if w.op in ("lse_dim0", "log_softmax_dim0"):
         R = w.shape[0]
         inner = w.numel // R
         cols = min(inner, rows * 4096)
-        return inputs_dev["x"].view(R, inner)[:, :cols].cpu().contiguous(), 4096
+        return {"x": inputs_dev["x"].view(R, inner)[:, :cols].cpu().contiguous()}, 4096
     y = inputs_dev["y"][:max(1, rows // 64)].cpu().contiguous()
-    return (y, inputs_dev["gamma"].cpu(), inputs_dev["beta"].cpu()), 1
+    return {"y": y, "gamma": inputs_dev["gamma"].cpu(), "beta": inputs_dev["beta"].cpu()}, 1
+
+
+def sample_text(w: synth.Workload, sample, units: int) -> str:
+    if w.op in ("log_softmax", "softmax"):
+        return f"{units} row passes over the first {sample['x'].shape[0]} rows x {w.shape[1]}"
+    if w.op in ("lse_dim0", "log_softmax_dim0"):
+        return (f"{units} passes of R={w.shape[0]} x 4096 columns over the first "
+                f"{sample['x'].shape[1]} columns")
+    return (f"{units} sample passes over the first {sample['y'].shape[0]} samples of "
+            f"{list(w.shape[1:])}")
 
 
 # ------------------------------------------------------------------ arms
@@ -302,10 +346,10 @@ def run_reference(args, w: synth.Workload):
     oracle.build()
     shape = list(w.shape)
     # one step = a bounded sample: 4 rows / 4096x32 columns / 1 sample
-    if w.op == "log_softmax":
+    if w.op in ("log_softmax", "softmax"):
         shape[0] = min(shape[0], 4)
         sample = f"{shape[0]} rows of {w.shape[1]}"
-    elif w.op == "lse_dim0":
+    elif w.op in ("lse_dim0", "log_softmax_dim0"):
         shape[1:] = [1, min(w.numel // w.shape[0], 4096 * 32)]
         sample = f"R={w.shape[0]} x {shape[2]} columns"
     else:
@@ -315,17 +359,7 @@ def run_reference(args, w: synth.Workload):
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        if w.op == "log_softmax":
-            oracle.log_softmax(inputs["x"])
-            nbytes = 8 * inputs["x"].numel()
-        elif w.op == "lse_dim0":
-            x = inputs["x"].reshape(shape[0], -1)
-            oracle.lse_reduce(x, 1, x.shape[0], x.shape[1])
-            nbytes = 4 * (x.numel() + x.shape[1])
-        else:
-            oracle.gn_act_lse(inputs["y"], inputs["gamma"], inputs["beta"], w.params["G"], w.params["eps"])
-            y = inputs["y"]
-            nbytes = 4 * (y.numel() + y.shape[0] * y.shape[2] * y.shape[3])
+        nbytes = oracle_call(w, inputs)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -443,11 +477,9 @@ def run_ours(args, w: synth.Workload):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        sample, unit_rows = oracle_sample(w, inputs, 256)
-        b, s, units = time_oracle(w, sample, budget_s=args.cpu_seconds, unit_rows=unit_rows)
-        what = {"log_softmax": f"{units} row passes over the first {sample.shape[0] if hasattr(sample, 'shape') else 0} rows x {w.shape[1]}",
-                "lse_dim0": f"{units} passes of R={w.shape[0]} x 4096 columns over the first {sample.shape[1] if hasattr(sample, 'shape') else 0} columns",
-                "gn_act_lse": f"{units} sample passes over the first {sample[0].shape[0] if isinstance(sample, tuple) else 0} samples of [64,126,126]"}[w.op]
+        sample, unit = oracle_sample(w, inputs, 256)
+        b, s, units = time_oracle(w, sample, budget_s=args.cpu_seconds, unit=unit)
+        what = sample_text(w, sample, units)
         cpu = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": what + f", {s:.1f} s single-threaded"}
 
@@ -491,11 +523,17 @@ def run_e2e(L, w: synth.Workload, inputs, args, dev, world):
     def one():
         if w.op == "log_softmax":
             L.log_softmax(host_in["x"], out=host_out)
+        elif w.op == "softmax":
+            L.softmax(host_in["x"], out=host_out)
         elif w.op == "lse_dim0":
             L.logsumexp(host_in["x"], dim=0, out=host_out)
+        elif w.op == "log_softmax_dim0":
+            L.log_softmax(host_in["x"], out=host_out, dim=0)
         else:
-            L.gn_act_lse_forward(host_in["y"], host_in["gamma"], host_in["beta"], w.params["G"],
-                                 w.params["eps"], out=host_out)
+            fn = {"gn_act_lse": L.gn_act_lse_forward, "group_norm": L.group_norm_forward,
+                  "gn_act_residual": L.gn_act_residual_forward}[w.op]
+            fn(host_in["y"], host_in["gamma"], host_in["beta"], w.params["G"], w.params["eps"],
+               out=host_out)
 
     one()
     torch.cuda.synchronize(dev)

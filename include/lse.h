@@ -103,6 +103,64 @@ lse_status_t log_softmax_lastdim_host(const float* x, float* out, int64_t rows, 
                                       cudaStream_t stream);
 
 /*
+ * softmax_lastdim — row-wise softmax of a contiguous (rows, cols) tensor, the
+ * non-log variant that "Kimi-K2.6 / l1_p24" describes beside log_softmax (in
+ * its discussion of how the write pass differs: exp(x - max) scaled by 1/sum):
+ *     out[r, j] = exp(x[r, j] - lse over k of x[r, k]),
+ * which equals exp(x - max) / sum up to rounding.  It is exp of
+ * log_softmax_lastdim's result, special values included: a row holding NaN,
+ * +inf, or only -inf gives NaN where log_softmax does, and 0 where log_softmax
+ * gives -inf.  Same arguments, layout, staging and rules as
+ * log_softmax_lastdim.  Accuracy: |err| <= 2e-5 + 1e-6 * |ref|.
+ */
+lse_status_t softmax_lastdim(const float* x, float* out, int64_t rows, int64_t cols,
+                             cudaStream_t stream);
+
+/*
+ * log_softmax_dim — log_softmax over the middle axis of a contiguous
+ * (outer, R, inner) tensor, the log_softmax identity of "Kimi-K2.6 / l1_p24"
+ * (opening analysis) along an axis of stride `inner`:
+ *     out[o, r, i] = x[o, r, i] - lse over r' of x[o, r', i].
+ * log_softmax(x, dim=d) of any contiguous tensor is this call with
+ * outer = prod(shape[:d]), R = shape[d], inner = prod(shape[d+1:]); inner = 1
+ * is log_softmax_lastdim.  For inner > 1 one kernel computes the lse of a tile
+ * of columns (the reduction of lse_reduce) and then writes the tile, whose
+ * second read is served from L2 while the tiles in flight fit there.
+ *   x    [outer * R * inner] fp32, device, read only.
+ *   out  [outer * R * inner] fp32, device, written (must not alias x).
+ *   outer, R, inner >= 0.
+ */
+lse_status_t log_softmax_dim(const float* x, float* out, int64_t outer, int64_t R, int64_t inner,
+                             cudaStream_t stream);
+
+/*
+ * group_norm — GroupNorm forward alone, materialised ("Kimi-K2.6 / l2_p92",
+ * GroupNorm discussion), the first step of gn_act_lse's chain:
+ *   out[n,c,p] = (y[n,c,p] - mean[n,g]) / sqrt(var[n,g] + eps) * gamma[c] + beta[c]
+ * with mean and population variance over the C/G channels of group g of
+ * sample n and all HW positions.
+ *   y      [N * C * HW] fp32 NCHW, device, read only.
+ *   gamma  [C], beta [C] fp32, device, read only.
+ *   out    [N * C * HW] fp32, device, written (must not alias y).
+ *   N >= 0, HW >= 0, 1 <= C <= 8192, G >= 1, C % G == 0; eps >= 0 and finite.
+ * One cooperative kernel: the statistics of a sample, then its normalised
+ * output written from a second read of the sample served by L2.  Scratch and
+ * error rules as gn_act_lse.
+ */
+lse_status_t group_norm(const float* y, const float* gamma, const float* beta, float* out,
+                        int64_t N, int64_t C, int64_t HW, int64_t G, float eps,
+                        cudaStream_t stream);
+
+/*
+ * gn_act_residual — gn_act_lse's chain without the final reduction
+ * ("Kimi-K2.6 / l2_p92"): out[n,c,p] = y[n,c,p] + hardswish(tanh(z[n,c,p])),
+ * z the group_norm output.  Arguments, sizes and rules as group_norm.
+ */
+lse_status_t gn_act_residual(const float* y, const float* gamma, const float* beta, float* out,
+                             int64_t N, int64_t C, int64_t HW, int64_t G, float eps,
+                             cudaStream_t stream);
+
+/*
  * gn_act_lse — GroupNorm -> tanh -> hardswish -> residual add -> logsumexp over
  * channels, keepdim ("Kimi-K2.6 / l2_p92", the chain after its Conv2d):
  *   mean[n,g], var[n,g] : population statistics of the C/G channels of group g
@@ -113,9 +171,10 @@ lse_status_t log_softmax_lastdim_host(const float* x, float* out, int64_t rows, 
  *   y      [N * C * HW] fp32 NCHW, device, read only.
  *   gamma  [C], beta [C] fp32, device, read only.
  *   out    [N * HW] fp32, device, written.
- *   N >= 0, HW >= 0, C >= 1, G >= 1, C % G == 0; eps >= 0 and finite.
- * The per-(n, g) statistics need 2*N*G floats of scratch.  The library takes
- * them, stream-ordered, from a memory pool it owns on the current device
+ *   N >= 0, HW >= 0, 1 <= C <= 8192, G >= 1, C % G == 0; eps >= 0 and finite.
+ * The per-(n, g) statistics and a work counter need 16*N*G + 4*N + 32 bytes of
+ * scratch.  The library takes them, stream-ordered, from a memory pool it owns
+ * on the current device
  * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`), so concurrent calls on
  * different streams never share scratch.  lse_release_workspace() returns the
  * pool's idle memory to the device.

@@ -8,9 +8,17 @@ library is missing or the device is not supported, calls raise.
 C-ABI entry points (declared in include/lse.h), same names here:
     lse_reduce(x, out, outer, R, inner, stream=None)
     log_softmax_lastdim(x, out, rows, cols, stream=None)
+    log_softmax_lastdim_host(x, out, rows, cols, stream=None)   (host tensors)
+    softmax_lastdim(x, out, rows, cols, stream=None)
+    log_softmax_dim(x, out, outer, R, inner, stream=None)
     gn_act_lse(y, gamma, beta, out, N, C, HW, G, eps, stream=None)
+    gn_act_lse_noalloc(y, gamma, beta, out, N, C, HW, G, eps, stream=None)
+    group_norm(y, gamma, beta, out, N, C, HW, G, eps, stream=None)
+    gn_act_residual(y, gamma, beta, out, N, C, HW, G, eps, stream=None)
 Conveniences that allocate the output with torch:
-    logsumexp(x, dim=0), log_softmax(x), gn_act_lse_forward(y, gamma, beta, G, eps)
+    logsumexp(x, dim=0), log_softmax(x, dim=-1), softmax(x),
+    gn_act_lse_forward(y, gamma, beta, G, eps), group_norm_forward(...),
+    gn_act_residual_forward(...)
 """
 from __future__ import annotations
 
@@ -28,8 +36,10 @@ STATUS = {
     5: "LSE_ERR_UNSUPPORTED", 6: "LSE_ERR_VALUE", 7: "LSE_ERR_TIMEOUT",
 }
 
-EXPORTS = ("lse_reduce", "log_softmax_lastdim", "gn_act_lse", "lse_release_workspace",
-           "lse_device_status", "lse_status_string", "lse_last_cuda_error", "lse_version")
+EXPORTS = ("lse_reduce", "log_softmax_lastdim", "log_softmax_lastdim_host", "softmax_lastdim",
+           "log_softmax_dim", "gn_act_lse", "gn_act_lse_noalloc", "group_norm", "gn_act_residual",
+           "lse_release_workspace", "lse_device_status", "lse_status_string", "lse_last_cuda_error",
+           "lse_version")
 
 
 class LseError(RuntimeError):
@@ -57,7 +67,11 @@ def load_library(path: str = LIB_PATH):
     lib.log_softmax_lastdim.argtypes = [vp, vp, i64, i64, vp]
     lib.log_softmax_lastdim_host.argtypes = [vp, vp, i64, i64, vp]
     lib.log_softmax_lastdim_host.restype = ctypes.c_int
+    lib.softmax_lastdim.argtypes = [vp, vp, i64, i64, vp]
+    lib.log_softmax_dim.argtypes = [vp, vp, i64, i64, i64, vp]
     lib.gn_act_lse.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
+    lib.group_norm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
+    lib.gn_act_residual.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
     lib.gn_act_lse_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
     lib.gn_act_lse_noalloc.restype = ctypes.c_int
     lib.lse_release_workspace.argtypes = []
@@ -66,7 +80,8 @@ def load_library(path: str = LIB_PATH):
     lib.lse_status_string.restype = ctypes.c_char_p
     lib.lse_last_cuda_error.argtypes = []
     lib.lse_version.argtypes = []
-    for name in ("lse_reduce", "log_softmax_lastdim", "gn_act_lse", "lse_release_workspace",
+    for name in ("lse_reduce", "log_softmax_lastdim", "softmax_lastdim", "log_softmax_dim",
+                 "gn_act_lse", "group_norm", "gn_act_residual", "lse_release_workspace",
                  "lse_device_status", "lse_last_cuda_error", "lse_version"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -134,6 +149,23 @@ def log_softmax_lastdim(x, out, rows: int, cols: int, stream=None) -> None:
     _check("log_softmax_lastdim", rc)
 
 
+def softmax_lastdim(x, out, rows: int, cols: int, stream=None) -> None:
+    """out[r, j] = exp(x[r, j] - logsumexp_k x[r, k]) over a contiguous (rows, cols) tensor."""
+    lib = load_library()
+    with _device_of(x):
+        rc = lib.softmax_lastdim(_ptr(x), _ptr(out), int(rows), int(cols), _stream(stream, x))
+    _check("softmax_lastdim", rc)
+
+
+def log_softmax_dim(x, out, outer: int, R: int, inner: int, stream=None) -> None:
+    """out[o, r, i] = x[o, r, i] - logsumexp over r' of x[o, r', i]; x and out (outer, R, inner)."""
+    lib = load_library()
+    with _device_of(x):
+        rc = lib.log_softmax_dim(_ptr(x), _ptr(out), int(outer), int(R), int(inner),
+                                 _stream(stream, x))
+    _check("log_softmax_dim", rc)
+
+
 def _host_ptr(t):
     if not isinstance(t, torch.Tensor) or t.is_cuda:
         raise ValueError("expected a CPU tensor")
@@ -159,6 +191,26 @@ def gn_act_lse(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: float,
         rc = lib.gn_act_lse(_ptr(y), _ptr(gamma), _ptr(beta), _ptr(out), int(N), int(C), int(HW),
                             int(G), float(eps), _stream(stream, y))
     _check("gn_act_lse", rc)
+
+
+def group_norm(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: float,
+               stream=None) -> None:
+    """GroupNorm forward with per-channel affine; out has y's shape [N, C, HW]."""
+    lib = load_library()
+    with _device_of(y):
+        rc = lib.group_norm(_ptr(y), _ptr(gamma), _ptr(beta), _ptr(out), int(N), int(C), int(HW),
+                            int(G), float(eps), _stream(stream, y))
+    _check("group_norm", rc)
+
+
+def gn_act_residual(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: float,
+                    stream=None) -> None:
+    """y + hardswish(tanh(GroupNorm(y))); out has y's shape [N, C, HW]."""
+    lib = load_library()
+    with _device_of(y):
+        rc = lib.gn_act_residual(_ptr(y), _ptr(gamma), _ptr(beta), _ptr(out), int(N), int(C),
+                                 int(HW), int(G), float(eps), _stream(stream, y))
+    _check("gn_act_residual", rc)
 
 
 def gn_act_lse_noalloc(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: float,
@@ -244,9 +296,27 @@ def logsumexp(x: torch.Tensor, dim: int = 0, keepdim: bool = False, out=None,
     return _result(res, host, out)
 
 
-def log_softmax(x: torch.Tensor, out=None, device="cuda") -> torch.Tensor:
-    """log_softmax over the last axis of fp32 x (any leading shape).  CPU input is copied
-    to `device` and the result back to host memory (`out` if given)."""
+def _split(shape, dim):
+    """(outer, R, inner) of a contiguous tensor of `shape` around axis `dim`."""
+    outer = 1
+    for s in shape[:dim]:
+        outer *= s
+    inner = 1
+    for s in shape[dim + 1:]:
+        inner *= s
+    return outer, (shape[dim] if shape else 1), inner
+
+
+def log_softmax(x: torch.Tensor, out=None, device="cuda", *, dim: int = -1) -> torch.Tensor:
+    """log_softmax of fp32 x over axis `dim` (default the last).  CPU input is copied
+    to `device` and the result back to host memory (`out` if given); for the last
+    axis the copies are pipelined with the computation by the library."""
+    if x.ndim and dim % x.ndim != x.ndim - 1:
+        xd, host = _to_device(x, device)
+        outer, R, inner = _split(list(xd.shape), dim % xd.ndim)
+        res = _device_out(xd.shape, xd, host, out)
+        log_softmax_dim(xd, res, outer, R, inner)
+        return _result(res, host, out)
     if not x.is_cuda:
         # host in, host out: the library pipelines chunks through the device
         xh = x.contiguous()
@@ -265,6 +335,41 @@ def log_softmax(x: torch.Tensor, out=None, device="cuda") -> torch.Tensor:
     res = _device_out(xd.shape, xd, host, out)
     log_softmax_lastdim(xd, res, rows, cols)
     return _result(res, host, out)
+
+
+def softmax(x: torch.Tensor, out=None, device="cuda") -> torch.Tensor:
+    """softmax over the last axis of fp32 x (any leading shape), as exp(x - logsumexp)."""
+    xd, host = _to_device(x, device)
+    cols = xd.shape[-1] if xd.ndim else 1
+    rows = xd.numel() // cols if cols else 0
+    res = _device_out(xd.shape, xd, host, out)
+    softmax_lastdim(xd, res, rows, cols)
+    return _result(res, host, out)
+
+
+def _gn_call(fn, y, gamma, beta, G, eps, out, device):
+    yd, host = _to_device(y, device)
+    gd, _ = _to_device(gamma, yd.device)
+    bd, _ = _to_device(beta, yd.device)
+    N, C = yd.shape[0], yd.shape[1]
+    HW = 1
+    for s in yd.shape[2:]:
+        HW *= s
+    res = _device_out(yd.shape, yd, host, out)
+    fn(yd, gd, bd, res, N, C, HW, G, eps)
+    return _result(res, host, out)
+
+
+def group_norm_forward(y: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, G: int,
+                       eps: float = 1e-5, out=None, device="cuda") -> torch.Tensor:
+    """GroupNorm(G, eps) with affine gamma/beta of y [N, C, *spatial]; same shape out."""
+    return _gn_call(group_norm, y, gamma, beta, G, eps, out, device)
+
+
+def gn_act_residual_forward(y: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, G: int,
+                            eps: float = 1e-5, out=None, device="cuda") -> torch.Tensor:
+    """y + hardswish(tanh(GroupNorm(y))) for y [N, C, *spatial]; same shape out."""
+    return _gn_call(gn_act_residual, y, gamma, beta, G, eps, out, device)
 
 
 def gn_act_lse_forward(y: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, G: int,

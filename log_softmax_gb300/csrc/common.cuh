@@ -90,6 +90,22 @@ __device__ __forceinline__ void ms_fold(MS& st, const float (&v)[K]) {
     st.s += acc0 + acc1;
 }
 
+// Output of a row transform for one element: x - lse (log_softmax) or
+// exp(x - lse) (softmax, as 2^((x - lse) log2 e); -inf gives 0, and the NaN
+// cases of x - lse stay NaN).
+template <bool SOFTMAX>
+__device__ __forceinline__ float row_out(float v, float lse) {
+    if constexpr (SOFTMAX) return ex2((v - lse) * kLog2e);
+    return v - lse;
+}
+
+__device__ __forceinline__ float4 row_out4(float4 q, float lse, bool softmax) {
+    if (softmax)
+        return make_float4(row_out<true>(q.x, lse), row_out<true>(q.y, lse), row_out<true>(q.z, lse),
+                           row_out<true>(q.w, lse));
+    return make_float4(q.x - lse, q.y - lse, q.z - lse, q.w - lse);
+}
+
 // lse from the final pair, with the special-value rules: NaN, then +inf, then
 // the empty / all -inf set gives -inf.
 __device__ __forceinline__ float ms_lse(MS st) {
@@ -175,6 +191,12 @@ __device__ __forceinline__ float4 ld_f4_l2hint(const float* p, uint64_t policy) 
     asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(p), "l"(policy));
+    return v;
+}
+
+__device__ __forceinline__ float ld_f1_l2hint(const float* p, uint64_t policy) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
     return v;
 }
 

@@ -199,6 +199,36 @@ __device__ __forceinline__ void apply_pixels(const float* __restrict__ yp, const
     }
 }
 
+// Elementwise outputs of one thread's VEC adjacent pixels of one sample, every
+// channel plane in turn (coalesced 128-bit loads and stores across the warp):
+//   OUT 1  z = (v - mean) * rstd * gamma + beta          tab[c] = {mean, rstd*gamma, beta, 0}
+//   OUT 2  v + hardswish(tanh(z))                        tab[c] = {mean, rstd*gamma*2log2e, beta*2log2e, 0}
+template <int VEC, int OUT, int CH = 4>
+__device__ __forceinline__ void write_pixels(const float* __restrict__ yp, const float4* tab, int C, int64_t HW,
+                                             float* __restrict__ dst, uint64_t policy) {
+    auto f = [](float v, float4 e) { return OUT == 1 ? fmaf(v - e.x, e.y, e.z) : act_residual(v, e); };
+    auto put = [&](int c, const float (&v)[VEC]) {
+        const float4 e = tab[c];
+        if constexpr (VEC == 4)
+            st_stream_f4(dst + (int64_t)c * HW, make_float4(f(v[0], e), f(v[1], e), f(v[2], e), f(v[3], e)));
+        else
+            st_stream_f1(dst + (int64_t)c * HW, f(v[0], e));
+    };
+    int c = 0;
+    for (; c + CH <= C; c += CH) {
+        float v[CH][VEC];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) load_vec<VEC, true>(yp + (int64_t)(c + k) * HW, v[k], policy);
+#pragma unroll
+        for (int k = 0; k < CH; ++k) put(c + k, v[k]);
+    }
+    for (; c < C; ++c) {
+        float v[VEC];
+        load_vec<VEC, true>(yp + (int64_t)c * HW, v, policy);
+        put(c, v);
+    }
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(128) gn_apply_kernel(const float* __restrict__ y,
                                                        const float* __restrict__ gamma,
@@ -293,7 +323,11 @@ struct GnFusedArgs {
 // (the grid is cooperative: all CTAs resident) and wait on nothing, so the wait
 // ends.  The lag keeps each sample's second read close behind its first, while
 // the sample (4 MB at 64 x 126 x 126) is still in L2: HBM sees y once.
-template <int VEC, int T>
+//
+// OUT selects what an apply tile writes: 0 the channel lse (out is N x HW),
+// 1 the GroupNorm output z, 2 the chain before the lse, y + hardswish(tanh(z))
+// (both N x C x HW).
+template <int VEC, int T, int OUT>
 __global__ void __launch_bounds__(T) gn_fused_kernel(const GnFusedArgs a) {
     extern __shared__ float4 tab[];  // [C] {mean, rstd*gamma*2log2e, beta*2log2e, 0}
     __shared__ Welford red[32];
@@ -375,12 +409,18 @@ __global__ void __launch_bounds__(T) gn_fused_kernel(const GnFusedArgs a) {
                     acc = wf_merge(acc, Welford{q.x, q.y, q.z});
                 }
                 const float rstd = 1.f / sqrtf(acc.m2 / acc.n + a.eps);
-                tab[c] = make_float4(acc.mean, rstd * a.gamma[c] * (2.f * kLog2e), a.beta[c] * (2.f * kLog2e), 0.f);
+                const float sc = OUT == 1 ? 1.f : 2.f * kLog2e;
+                tab[c] = make_float4(acc.mean, rstd * a.gamma[c] * sc, a.beta[c] * sc, 0.f);
             }
             __syncthreads();
             const int64_t p0 = (idx * T + tid) * VEC;
-            if (p0 < HW)
-                apply_pixels<VEC, true>(a.y + n * (int64_t)C * HW + p0, tab, C, HW, a.out + n * HW + p0, drop);
+            if (p0 < HW) {
+                const float* yp = a.y + n * (int64_t)C * HW + p0;
+                if constexpr (OUT == 0)
+                    apply_pixels<VEC, true>(yp, tab, C, HW, a.out + n * HW + p0, drop);
+                else
+                    write_pixels<VEC, OUT>(yp, tab, C, HW, a.out + n * (int64_t)C * HW + p0, drop);
+            }
         }
     }
 }
@@ -436,9 +476,9 @@ size_t gn_fused_scratch_bytes(int64_t N, int64_t G) {
     return (size_t)N * G * gn_parts() * sizeof(float4) + ((size_t)N * sizeof(unsigned) + 15) / 16 * 16 + 16;
 }
 
-template <int VEC, int T>
+template <int VEC, int T, int OUT = 0>
 static cudaError_t gn_fused_go(const DeviceInfo& dev, const GnFusedArgs& args, size_t smem, cudaStream_t stream) {
-    auto kern = gn_fused_kernel<VEC, T>;
+    auto kern = gn_fused_kernel<VEC, T, OUT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -468,7 +508,7 @@ static cudaError_t gn_fused_go(const DeviceInfo& dev, const GnFusedArgs& args, s
 
 cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const float* gamma,
                                     const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
-                                    int64_t G, float eps, void* scratch, cudaStream_t stream) {
+                                    int64_t G, float eps, void* scratch, cudaStream_t stream, int out_kind) {
     const bool vec = (HW % 4 == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0) &&
                      ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
     const int VEC = vec ? 4 : 1;
@@ -482,7 +522,7 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     args.C = (int)C;
     args.G = (int)G;
     args.parts = gn_parts();
-    const int T = env_int("LSE_GN_THREADS", 256);
+    const int T = out_kind == 0 ? env_int("LSE_GN_THREADS", 256) : 256;
     args.tiles = (int)((HW + (int64_t)T * VEC - 1) / ((int64_t)T * VEC));
     args.lag = (int)std::min<int64_t>(N, std::max(0, env_int("LSE_GN_LAG", 16)));
     args.eps = eps;
@@ -496,6 +536,8 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     cudaError_t e = cudaMemsetAsync(args.done, 0, done_bytes + 16, stream);
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)C * sizeof(float4);
+    if (out_kind == 1) return vec ? gn_fused_go<4, 256, 1>(dev, args, smem, stream) : gn_fused_go<1, 256, 1>(dev, args, smem, stream);
+    if (out_kind == 2) return vec ? gn_fused_go<4, 256, 2>(dev, args, smem, stream) : gn_fused_go<1, 256, 2>(dev, args, smem, stream);
     if (T == 1024) return vec ? gn_fused_go<4, 1024>(dev, args, smem, stream) : gn_fused_go<1, 1024>(dev, args, smem, stream);
     if (T == 512) return vec ? gn_fused_go<4, 512>(dev, args, smem, stream) : gn_fused_go<1, 512>(dev, args, smem, stream);
     return vec ? gn_fused_go<4, 256>(dev, args, smem, stream) : gn_fused_go<1, 256>(dev, args, smem, stream);

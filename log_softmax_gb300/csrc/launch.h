@@ -15,12 +15,14 @@ struct DeviceInfo {
     int* status = nullptr;    // device address of the library's status word
 };
 
-// Form 1: out[o, i] = lse over r of x[o, r, i] (inner > 1).
+// Form 1: out[o, i] = lse over r of x[o, r, i] (inner > 1).  With log_softmax
+// set, out[o, r, i] = x[o, r, i] - that lse instead (out has x's shape).
 cudaError_t launch_lse_strided(const DeviceInfo& dev, const float* x, float* out, int64_t outer,
-                               int64_t R, int64_t inner, cudaStream_t stream);
+                               int64_t R, int64_t inner, cudaStream_t stream, bool log_softmax = false);
 
 // Form 2, rows held in registers (cols up to kRegRowMaxCols).  mode 0 writes
-// log_softmax into out (rows x cols); mode 1 writes the row lse into out (rows).
+// log_softmax into out (rows x cols); mode 1 writes the row lse into out (rows);
+// mode 2 writes softmax into out (rows x cols).
 constexpr int64_t kRegRowMaxCols = 32768;
 cudaError_t launch_rows_reg(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
                             int64_t cols, int mode, cudaStream_t stream);
@@ -51,7 +53,8 @@ cudaError_t launch_lsm_smem_group(const DeviceInfo& dev, const float* x, float* 
 cudaError_t plan_lsm_ws_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
                               int64_t cols, GroupPlan* plan);
 cudaError_t launch_lsm_ws_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
-                                int64_t cols, const GroupPlan& plan, void* scratch, cudaStream_t stream);
+                                int64_t cols, const GroupPlan& plan, void* scratch, cudaStream_t stream,
+                                bool softmax = false);
 
 // Form 2, rows split over a group of CTAs of a cooperative grid that read their
 // slices twice, the second time from L2.  Same plan / scratch protocol.
@@ -74,10 +77,13 @@ cudaError_t launch_gn_act_lse(const DeviceInfo& dev, const float* y, const float
 // Form 3 in one cooperative kernel: statistics parts and apply tiles of the
 // samples claimed from one work queue, each sample's second read close behind
 // its first so that it hits L2.  Scratch: gn_fused_scratch_bytes(N, G).
+// out_kind 0 writes the channel lse (N x HW); 1 the GroupNorm output and 2 the
+// chain before the lse, y + hardswish(tanh(GroupNorm(y))) (both N x C x HW).
 size_t gn_fused_scratch_bytes(int64_t N, int64_t G);
 cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const float* gamma,
                                     const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
-                                    int64_t G, float eps, void* scratch, cudaStream_t stream);
+                                    int64_t G, float eps, void* scratch, cudaStream_t stream,
+                                    int out_kind = 0);
 
 // Largest C that the apply kernel's shared-memory table holds.
 constexpr int64_t kGnMaxChannels = 8192;

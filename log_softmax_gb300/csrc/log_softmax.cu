@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(1024) rows_reg_kernel(const float* __restrict_
             s = warp_allsum(lane < nwarps ? red[lane] : 0.f);
         }
         const float lse = lse_from_max_sum(m, s);
-        if constexpr (MODE == 0) {
+        if constexpr (MODE != 1) {
+            constexpr bool SM = (MODE == 2);
             if (rv) {
                 float* dst = out + row * cols;
 #pragma unroll
@@ -113,10 +114,10 @@ __global__ void __launch_bounds__(1024) rows_reg_kernel(const float* __restrict_
                     const int64_t j = ((int64_t)k * GT + t) * VEC;
                     if (j < cols) {
                         if constexpr (VEC == 4) {
-                            st_stream_f4(dst + j, make_float4(v[k][0] - lse, v[k][1] - lse,
-                                                              v[k][2] - lse, v[k][3] - lse));
+                            st_stream_f4(dst + j, make_float4(row_out<SM>(v[k][0], lse), row_out<SM>(v[k][1], lse),
+                                                              row_out<SM>(v[k][2], lse), row_out<SM>(v[k][3], lse)));
                         } else {
-                            st_stream_f1(dst + j, v[k][0] - lse);
+                            st_stream_f1(dst + j, row_out<SM>(v[k][0], lse));
                         }
                     }
                 }
@@ -167,6 +168,7 @@ cudaError_t launch_rows_reg(const DeviceInfo& dev, const float* x, float* out, i
     if (cols > kRegRowMaxCols || (!vec4 && cols > 1024 * 16))
         return launch_rows_stream(dev, x, out, rows, cols, mode, stream);
     if (mode == 0) return rows_reg_dispatch<0>(dev, x, out, rows, cols, vec4, stream);
+    if (mode == 2) return rows_reg_dispatch<2>(dev, x, out, rows, cols, vec4, stream);
     return rows_reg_dispatch<1>(dev, x, out, rows, cols, vec4, stream);
 }
 
@@ -195,6 +197,7 @@ struct SmemRowArgs {
     // group variant only
     int group_size;            // CTAs per row; CTA b is rank b % group_size of group b / group_size
     unsigned long long* slots; // [groups][2][group_size] tagged pairs, all bytes 0xFF at launch
+    int softmax;               // warp-specialised kernel: write exp(x - lse) instead of x - lse
 };
 
 // Polls a tagged slot until its tag is `tag`, at most ~1 s / 2^26 polls; on
@@ -579,9 +582,10 @@ __global__ void __launch_bounds__(32 * (FW + SW), 1) lsm_ws_kernel(const SmemRow
                 const int cb = c * chunk;
                 const int n4 = std::min(chunk, len - cb) >> 2;
                 const float4* p = reinterpret_cast<const float4*>(buf + cb);
-                for (int i = sid; i < n4; i += NS) {
-                    float4 q = p[i];
-                    st_stream_f4(dst + cb + 4 * i, make_float4(q.x - lse, q.y - lse, q.z - lse, q.w - lse));
+                if (a.softmax) {
+                    for (int i = sid; i < n4; i += NS) st_stream_f4(dst + cb + 4 * i, row_out4(p[i], lse, true));
+                } else {
+                    for (int i = sid; i < n4; i += NS) st_stream_f4(dst + cb + 4 * i, row_out4(p[i], lse, false));
                 }
                 named_bar_sync(2, NS);  // every store warp is done reading chunk c (and lse_s)
                 if (sid == 0) issue(j + NB, c);
@@ -973,7 +977,8 @@ static cudaError_t ws_go_nb(int fw, int sw, const SmemRowArgs& args, const Group
 }
 
 cudaError_t launch_lsm_ws_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows,
-                                int64_t cols, const GroupPlan& p, void* scratch, cudaStream_t stream) {
+                                int64_t cols, const GroupPlan& p, void* scratch, cudaStream_t stream,
+                                bool softmax) {
     cudaError_t e = cudaMemsetAsync(scratch, 0xFF, p.scratch_bytes, stream);
     if (e != cudaSuccess) return e;
     const int nb = p.nbuf / 10000, fw = (p.nbuf / 100) % 100, sw = p.nbuf % 100;
@@ -981,7 +986,7 @@ cudaError_t launch_lsm_ws_group(const DeviceInfo& dev, const float* x, float* ou
         fprintf(stderr, "[lse] lsm_ws group: GS=%d groups=%d buffers=%d fold_warps=%d store_warps=%d "
                 "slice=%d chunk=%d smem=%zu\n", p.group_size, p.groups, nb, fw, sw, p.slice, p.chunk, p.smem);
     SmemRowArgs args{x, out, rows, cols, p.slice, p.chunk, dev.status, p.group_size,
-                     static_cast<unsigned long long*>(scratch)};
+                     static_cast<unsigned long long*>(scratch), softmax ? 1 : 0};
     switch (nb) {
         case 2: return ws_go_nb<2>(fw, sw, args, p, stream);
         case 4: return ws_go_nb<4>(fw, sw, args, p, stream);
@@ -1188,13 +1193,15 @@ __global__ void __launch_bounds__(512) rows_stream_kernel(const float* __restric
         if constexpr (MODE == 1) {
             if (rank == 0 && tid == 0) out[row] = lse;
         } else {
+            constexpr bool SM = (MODE == 2);
             float* dst = out + row * cols + c_begin;
             for (int64_t j = tid; j < n; j += T) {
                 if constexpr (VEC == 4) {
                     float4 a = ld_stream_f4(src + j * 4);
-                    st_stream_f4(dst + j * 4, make_float4(a.x - lse, a.y - lse, a.z - lse, a.w - lse));
+                    st_stream_f4(dst + j * 4, make_float4(row_out<SM>(a.x, lse), row_out<SM>(a.y, lse),
+                                                          row_out<SM>(a.z, lse), row_out<SM>(a.w, lse)));
                 } else {
-                    st_stream_f1(dst + j, ld_stream_f1(src + j) - lse);
+                    st_stream_f1(dst + j, row_out<SM>(ld_stream_f1(src + j), lse));
                 }
             }
         }
@@ -1238,9 +1245,11 @@ cudaError_t launch_rows_stream(const DeviceInfo& dev, const float* x, float* out
     if (forced == 1 || forced == 2 || forced == 4 || forced == 8) CL = forced;
     if (vec4) {
         return mode == 0 ? rows_stream_go<4, 0>(dev, x, out, rows, cols, CL, stream)
+             : mode == 2 ? rows_stream_go<4, 2>(dev, x, out, rows, cols, CL, stream)
                          : rows_stream_go<4, 1>(dev, x, out, rows, cols, CL, stream);
     }
     return mode == 0 ? rows_stream_go<1, 0>(dev, x, out, rows, cols, CL, stream)
+         : mode == 2 ? rows_stream_go<1, 2>(dev, x, out, rows, cols, CL, stream)
                      : rows_stream_go<1, 1>(dev, x, out, rows, cols, CL, stream);
 }
 

@@ -154,14 +154,14 @@ lse_status_t lse_reduce(const float* x, float* out, int64_t outer, int64_t R, in
     return e == cudaSuccess ? LSE_OK : cuda_fail(e);
 }
 
-lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64_t cols,
-                                 cudaStream_t stream) {
-    if (rows < 0 || cols < 0) return LSE_ERR_SIZE;
-    int64_t n = 0;
-    if (!mul_ok(rows, cols, &n) || n > INT64_MAX / 4) return LSE_ERR_SIZE;
-    if (n == 0) return LSE_OK;
-    if (!x || !out) return LSE_ERR_NULL;
-    if (!aligned4(x) || !aligned4(out)) return LSE_ERR_ALIGN;
+}  // extern "C"
+
+namespace {
+
+// Row-wise log_softmax (softmax = false) or softmax (true) of a (rows, cols)
+// tensor, after the entry point's argument checks.
+lse_status_t row_transform(const float* x, float* out, int64_t rows, int64_t cols, bool softmax,
+                           cudaStream_t stream) {
     DeviceState* s = nullptr;
     lse_status_t st = device_state(&s);
     if (st != LSE_OK) return st;
@@ -169,9 +169,11 @@ lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64
     // LSE_LSM_VARIANT forces a kernel: 1 registers, 2 cluster shared memory,
     // 3 streaming, 4 lock-step group shared memory, 5 group with an L2 re-read,
     // 6 warp-specialised group shared memory (the default for long aligned rows).
-    const int force = env_int("LSE_LSM_VARIANT", 0);
+    // softmax has the register, streaming and warp-specialised kernels only.
+    int force = env_int("LSE_LSM_VARIANT", 0);
+    if (softmax && force != 1 && force != 3 && force != 6) force = 0;
     if ((force == 0 || force == 1) && cols <= kRegRowMaxCols) {
-        e = launch_rows_reg(s->info, x, out, rows, cols, 0, stream);
+        e = launch_rows_reg(s->info, x, out, rows, cols, softmax ? 2 : 0, stream);
     } else {
         e = cudaErrorNotSupported;
         if (force == 2) {
@@ -189,7 +191,7 @@ lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64
                 e = cudaMallocFromPoolAsync(&scratch, plan.scratch_bytes, pool, stream);
                 if (e != cudaSuccess) return cuda_fail(e);
                 e = kind == 5 ? launch_lsm_l2_group(s->info, x, out, rows, cols, plan, scratch, stream)
-                  : kind == 6 ? launch_lsm_ws_group(s->info, x, out, rows, cols, plan, scratch, stream)
+                  : kind == 6 ? launch_lsm_ws_group(s->info, x, out, rows, cols, plan, scratch, stream, softmax)
                               : launch_lsm_smem_group(s->info, x, out, rows, cols, plan, scratch, stream);
                 cudaError_t ef = cudaFreeAsync(scratch, stream);
                 if (e == cudaSuccess) e = ef;
@@ -197,15 +199,31 @@ lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64
         }
         if (e == cudaErrorNotSupported) {
             (void)cudaGetLastError();
-            e = launch_rows_stream(s->info, x, out, rows, cols, 0, stream);
+            e = launch_rows_stream(s->info, x, out, rows, cols, softmax ? 2 : 0, stream);
         }
     }
     return e == cudaSuccess ? LSE_OK : cuda_fail(e);
 }
 
-lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, float* out,
-                        int64_t N, int64_t C, int64_t HW, int64_t G, float eps,
-                        cudaStream_t stream) {
+// Host-side checks shared by the row entry points.
+lse_status_t check_rows(const float* x, const float* out, int64_t rows, int64_t cols, bool* empty) {
+    *empty = false;
+    if (rows < 0 || cols < 0) return LSE_ERR_SIZE;
+    int64_t n = 0;
+    if (!mul_ok(rows, cols, &n) || n > INT64_MAX / 4) return LSE_ERR_SIZE;
+    if (n == 0) {
+        *empty = true;
+        return LSE_OK;
+    }
+    if (!x || !out) return LSE_ERR_NULL;
+    if (!aligned4(x) || !aligned4(out)) return LSE_ERR_ALIGN;
+    return LSE_OK;
+}
+
+// Host-side checks shared by the GroupNorm entry points.
+lse_status_t check_gn(const float* y, const float* gamma, const float* beta, const float* out, int64_t N,
+                      int64_t C, int64_t HW, int64_t G, float eps, bool* empty) {
+    *empty = false;
     if (N < 0 || HW < 0 || C <= 0 || G <= 0 || C % G != 0) return LSE_ERR_SIZE;
     if (C > kGnMaxChannels) return LSE_ERR_SIZE;
     int64_t nchw = 0, nhw = 0, ng = 0;
@@ -213,26 +231,102 @@ lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, f
         !mul_ok(N, HW, &nhw) || !mul_ok(N, G, &ng))
         return LSE_ERR_SIZE;
     if (!(eps >= 0.f) || eps == __builtin_inff()) return LSE_ERR_VALUE;
-    if (nhw == 0) return LSE_OK;
+    if (nhw == 0) {
+        *empty = true;
+        return LSE_OK;
+    }
     if (!y || !gamma || !beta || !out) return LSE_ERR_NULL;
     if (!aligned4(y) || !aligned4(gamma) || !aligned4(beta) || !aligned4(out)) return LSE_ERR_ALIGN;
+    return LSE_OK;
+}
+
+// The one-kernel GroupNorm chain with output kind out_kind (0 channel lse,
+// 1 GroupNorm, 2 chain before the lse), scratch from the device pool.
+lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, float* out, int64_t N, int64_t C,
+                      int64_t HW, int64_t G, float eps, int out_kind, cudaStream_t stream) {
     DeviceState* s = nullptr;
     lse_status_t st = device_state(&s);
     if (st != LSE_OK) return st;
     cudaMemPool_t pool = nullptr;
     if ((st = device_pool(s, &pool)) != LSE_OK) return st;
+    void* scratch = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, gn_fused_scratch_bytes(N, G), pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_gn_act_lse_fused(s->info, y, gamma, beta, out, N, C, HW, G, eps, scratch, stream, out_kind);
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (ef != cudaSuccess) return cuda_fail(ef);
+    return LSE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lse_status_t log_softmax_lastdim(const float* x, float* out, int64_t rows, int64_t cols,
+                                 cudaStream_t stream) {
+    bool empty = false;
+    lse_status_t st = check_rows(x, out, rows, cols, &empty);
+    if (st != LSE_OK || empty) return st;
+    return row_transform(x, out, rows, cols, false, stream);
+}
+
+lse_status_t softmax_lastdim(const float* x, float* out, int64_t rows, int64_t cols, cudaStream_t stream) {
+    bool empty = false;
+    lse_status_t st = check_rows(x, out, rows, cols, &empty);
+    if (st != LSE_OK || empty) return st;
+    return row_transform(x, out, rows, cols, true, stream);
+}
+
+lse_status_t log_softmax_dim(const float* x, float* out, int64_t outer, int64_t R, int64_t inner,
+                             cudaStream_t stream) {
+    if (outer < 0 || R < 0 || inner < 0) return LSE_ERR_SIZE;
+    int64_t rows = 0, n = 0;
+    if (!mul_ok(outer, inner, &rows) || !mul_ok(rows, R, &n) || n > INT64_MAX / 4) return LSE_ERR_SIZE;
+    if (n == 0) return LSE_OK;
+    if (!x || !out) return LSE_ERR_NULL;
+    if (!aligned4(x) || !aligned4(out)) return LSE_ERR_ALIGN;
+    if (inner == 1) return row_transform(x, out, outer, R, false, stream);
+    DeviceState* s = nullptr;
+    lse_status_t st = device_state(&s);
+    if (st != LSE_OK) return st;
+    cudaError_t e = launch_lse_strided(s->info, x, out, outer, R, inner, stream, true);
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+}
+
+lse_status_t group_norm(const float* y, const float* gamma, const float* beta, float* out, int64_t N, int64_t C,
+                        int64_t HW, int64_t G, float eps, cudaStream_t stream) {
+    bool empty = false;
+    lse_status_t st = check_gn(y, gamma, beta, out, N, C, HW, G, eps, &empty);
+    if (st != LSE_OK || empty) return st;
+    return gn_fused(y, gamma, beta, out, N, C, HW, G, eps, 1, stream);
+}
+
+lse_status_t gn_act_residual(const float* y, const float* gamma, const float* beta, float* out, int64_t N,
+                             int64_t C, int64_t HW, int64_t G, float eps, cudaStream_t stream) {
+    bool empty = false;
+    lse_status_t st = check_gn(y, gamma, beta, out, N, C, HW, G, eps, &empty);
+    if (st != LSE_OK || empty) return st;
+    return gn_fused(y, gamma, beta, out, N, C, HW, G, eps, 2, stream);
+}
+
+lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, float* out,
+                        int64_t N, int64_t C, int64_t HW, int64_t G, float eps,
+                        cudaStream_t stream) {
+    bool empty = false;
+    lse_status_t st = check_gn(y, gamma, beta, out, N, C, HW, G, eps, &empty);
+    if (st != LSE_OK || empty) return st;
     // LSE_GN_VARIANT=1 selects the two-kernel path (statistics, then apply);
     // the default is the one-kernel chain that re-reads each sample from L2.
-    const bool fused = env_int("LSE_GN_VARIANT", 0) != 1;
-    const size_t bytes = fused ? gn_fused_scratch_bytes(N, G) : (size_t)ng * 2 * sizeof(float);
+    if (env_int("LSE_GN_VARIANT", 0) != 1) return gn_fused(y, gamma, beta, out, N, C, HW, G, eps, 0, stream);
+    DeviceState* s = nullptr;
+    if ((st = device_state(&s)) != LSE_OK) return st;
+    cudaMemPool_t pool = nullptr;
+    if ((st = device_pool(s, &pool)) != LSE_OK) return st;
     void* stats = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&stats, bytes, pool, stream);
+    cudaError_t e = cudaMallocFromPoolAsync(&stats, (size_t)N * G * 2 * sizeof(float), pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (fused)
-        e = launch_gn_act_lse_fused(s->info, y, gamma, beta, out, N, C, HW, G, eps, stats, stream);
-    else
-        e = launch_gn_act_lse(s->info, y, gamma, beta, out, N, C, HW, G, eps, static_cast<float*>(stats),
-                              stream);
+    e = launch_gn_act_lse(s->info, y, gamma, beta, out, N, C, HW, G, eps, static_cast<float*>(stats), stream);
     cudaError_t ef = cudaFreeAsync(stats, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     if (ef != cudaSuccess) return cuda_fail(ef);

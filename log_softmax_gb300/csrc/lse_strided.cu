@@ -9,6 +9,13 @@
 // updated online, once per batch of CH values ("Kimi-K2.6 / l1_p24",
 // online-softmax derivation).  When R is long and inner is short, TY thread
 // rows split R and their pairs are merged in shared memory.
+//
+// With LSM set the same kernel writes log_softmax over the strided axis
+// instead of the lse (out has x's shape): the block publishes its columns'
+// lse in shared memory, then walks its tile a second time and writes
+// x - lse.  The first walk marks its lines evict-last in L2 and the second
+// evict-first, so the second walk is served from L2 while the tiles resident
+// at once fit there; x is read from HBM once and out written once.
 #include <algorithm>
 
 #include "common.cuh"
@@ -16,13 +23,25 @@
 
 namespace lse {
 
-template <int VEC, int CH>
+template <int VEC>
+__device__ __forceinline__ void load_cols(const float* p, float (&v)[VEC], uint64_t pol, bool hint) {
+    if constexpr (VEC == 4) {
+        float4 a = hint ? ld_f4_l2hint(p, pol) : ld_stream_f4(p);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
+        v[0] = hint ? ld_f1_l2hint(p, pol) : ld_stream_f1(p);
+    }
+}
+
+template <int VEC, int CH, bool LSM>
 __global__ void __launch_bounds__(256) lse_strided_kernel(const float* __restrict__ x,
                                                           float* __restrict__ out, int64_t outer,
                                                           int64_t R, int64_t inner, int64_t tiles) {
     __shared__ MS red[256 * VEC];
+    __shared__ float lse_s[LSM ? 256 * VEC : 1];
     const int TX = blockDim.x, TY = blockDim.y;
     const int tx = threadIdx.x, ty = threadIdx.y;
+    const uint64_t keep = LSM ? l2_policy_evict_last() : 0;
     const int64_t nblk = outer * tiles;
     for (int64_t b = blockIdx.x; b < nblk; b += gridDim.x) {
         const int64_t o = b / tiles;
@@ -40,28 +59,22 @@ __global__ void __launch_bounds__(256) lse_strided_kernel(const float* __restric
                 float v[VEC][CH];
 #pragma unroll
                 for (int k = 0; k < CH; ++k) {
-                    const float* p = base + (r + (int64_t)k * TY) * inner;
-                    if constexpr (VEC == 4) {
-                        float4 a = ld_stream_f4(p);
-                        v[0][k] = a.x; v[1][k] = a.y; v[2][k] = a.z; v[3][k] = a.w;
-                    } else {
-                        v[0][k] = ld_stream_f1(p);
-                    }
+                    float w[VEC];
+                    load_cols<VEC>(base + (r + (int64_t)k * TY) * inner, w, keep, LSM);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) v[j][k] = w[j];
                 }
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) ms_fold<CH>(st[j], v[j]);
             }
             for (; r < R; r += TY) {
-                const float* p = base + r * inner;
-                float v[VEC][1];
-                if constexpr (VEC == 4) {
-                    float4 a = ld_stream_f4(p);
-                    v[0][0] = a.x; v[1][0] = a.y; v[2][0] = a.z; v[3][0] = a.w;
-                } else {
-                    v[0][0] = ld_stream_f1(p);
-                }
+                float w[VEC];
+                load_cols<VEC>(base + r * inner, w, keep, LSM);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) ms_fold<1>(st[j], v[j]);
+                for (int j = 0; j < VEC; ++j) {
+                    float v1[1] = {w[j]};
+                    ms_fold<1>(st[j], v1);
+                }
             }
         }
         if (TY > 1) {  // tree merge over the thread rows (TY is a power of two)
@@ -84,6 +97,32 @@ __global__ void __launch_bounds__(256) lse_strided_kernel(const float* __restric
                 for (int j = 0; j < VEC; ++j) st[j] = red[tx * VEC + j];
             }
             __syncthreads();  // red is reused by the next tile
+        }
+        if constexpr (LSM) {
+            // every thread row needs the lse of its columns for the write walk
+            if (ty == 0) {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) lse_s[tx * VEC + j] = ms_lse(st[j]);
+            }
+            __syncthreads();
+            if (valid) {
+                float l[VEC];
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) l[j] = lse_s[tx * VEC + j];
+                const uint64_t drop = l2_policy_evict_first();
+                const int64_t off = o * R * inner + c0;
+                for (int64_t r = ty; r < R; r += TY) {
+                    float w[VEC];
+                    load_cols<VEC>(x + off + r * inner, w, drop, true);
+                    float* dst = out + off + r * inner;
+                    if constexpr (VEC == 4)
+                        st_stream_f4(dst, make_float4(w[0] - l[0], w[1] - l[1], w[2] - l[2], w[3] - l[3]));
+                    else
+                        st_stream_f1(dst, w[0] - l[0]);
+                }
+            }
+            __syncthreads();  // lse_s is reused by the next tile
+            continue;
         }
         if (ty == 0 && valid) {
             float* dst = out + o * inner + c0;
@@ -109,33 +148,46 @@ static int pow2_ceil(int64_t v) {
     return p;
 }
 
+template <bool LSM>
+static void strided_go(bool vec4, int CH, unsigned grid, dim3 block, const float* x, float* out, int64_t outer,
+                       int64_t R, int64_t inner, int64_t tiles, cudaStream_t stream) {
+    if (vec4) {
+        if (CH == 8)
+            lse_strided_kernel<4, 8, LSM><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
+        else
+            lse_strided_kernel<4, 4, LSM><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
+    } else {
+        if (CH == 8)
+            lse_strided_kernel<1, 8, LSM><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
+        else
+            lse_strided_kernel<1, 4, LSM><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
+    }
+}
+
 cudaError_t launch_lse_strided(const DeviceInfo& dev, const float* x, float* out, int64_t outer,
-                               int64_t R, int64_t inner, cudaStream_t stream) {
+                               int64_t R, int64_t inner, cudaStream_t stream, bool log_softmax) {
     const bool vec4 = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0) &&
                       ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
     const int VEC = vec4 ? 4 : 1;
     const int64_t ncols = (inner + VEC - 1) / VEC;
-    const int TX = (int)std::min<int64_t>(256, std::max<int64_t>(32, pow2_ceil(ncols)));
     const int CH = (R >= 8) ? 8 : 4;
-    int TY = 256 / TX;
-    TY = std::min(TY, pow2_floor(std::max<int64_t>(1, R / CH)));
+    const int ty_cap = pow2_floor(std::max<int64_t>(1, R / CH));
+    // The log_softmax walk re-reads a tile of R x TX*VEC floats from L2, so it
+    // splits R over as many thread rows as it can (up to 8): fewer bytes per
+    // thread between the two walks, and a smaller set of tiles held in L2.
+    const int tx_max = log_softmax ? 256 / std::min(8, ty_cap) : 256;
+    const int TX = (int)std::min<int64_t>(tx_max, std::max<int64_t>(32, pow2_ceil(ncols)));
+    const int TY = std::min(256 / TX, ty_cap);
     const int64_t tiles = (ncols + TX - 1) / TX;
     const int64_t nblk = outer * tiles;
     const int per_sm = std::max(1, 2048 / (TX * TY));
     const int64_t cap = (int64_t)dev.sm_count * per_sm * 64;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nblk, cap));
     dim3 block(TX, TY);
-    if (vec4) {
-        if (CH == 8)
-            lse_strided_kernel<4, 8><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
-        else
-            lse_strided_kernel<4, 4><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
-    } else {
-        if (CH == 8)
-            lse_strided_kernel<1, 8><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
-        else
-            lse_strided_kernel<1, 4><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
-    }
+    if (log_softmax)
+        strided_go<true>(vec4, CH, grid, block, x, out, outer, R, inner, tiles, stream);
+    else
+        strided_go<false>(vec4, CH, grid, block, x, out, outer, R, inner, tiles, stream);
     return cudaGetLastError();
 }
 

@@ -53,7 +53,8 @@ def bernoulli_mask(shape, seed: int, p: float, device="cpu") -> torch.Tensor:
 class Workload:
     """A named workload: what is computed, on which shape, from which recipe."""
     name: str
-    op: str                      # "lse_dim0" | "log_softmax" | "gn_act_lse"
+    op: str                      # "lse_dim0" | "log_softmax" | "gn_act_lse" | "softmax" |
+                                 # "log_softmax_dim0" | "group_norm" | "gn_act_residual"
     shape: tuple
     recipe: str
     params: dict = field(default_factory=dict)
@@ -88,6 +89,18 @@ WORKLOADS = {
         {"seed": 5, "gamma_seed": 105, "beta_seed": 205, "G": 16, "eps": 1e-5}),
 }
 
+# The operations beside the hot path, each on the shape and recipe of the
+# hot-path workload it sits next to: softmax on the LogSoftmax rows,
+# log_softmax over dim 0 of the (R, B, D) tensor, and GroupNorm alone and the
+# chain without its lse on the conv output.
+for _name, _op, _like in (
+        ("softmax_4096x393216", "softmax", "log_softmax_4096x393216"),
+        ("log_softmax_dim0_32x8192x4096", "log_softmax_dim0", "lse_dim0_32x8192x4096"),
+        ("group_norm_128x64x126x126", "group_norm", "gn_act_lse_128x64x126x126"),
+        ("gn_act_residual_128x64x126x126", "gn_act_residual", "gn_act_lse_128x64x126x126")):
+    _w = WORKLOADS[_like]
+    WORKLOADS[_name] = Workload(_name, _op, _w.shape, _w.recipe, dict(_w.params, like=_like))
+
 
 def make_inputs(w: Workload | str, device="cpu", shape=None):
     """Draw the inputs of a workload (optionally at another shape, same recipe).
@@ -98,7 +111,7 @@ def make_inputs(w: Workload | str, device="cpu", shape=None):
         w = WORKLOADS[w]
     shape = tuple(shape) if shape is not None else w.shape
     p = w.params
-    base = w.name.split("@")[0]
+    base = p.get("like", w.name.split("@")[0])
     if base == "lse_dim0_4x10x32":
         return {"x": normal(shape, p["seed"], device=device)}
     if base == "log_softmax_256x4096":

@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("lse_reduce", "log_softmax_lastdim", "gn_act_lse", "lse_status_string",
-              "lse_last_cuda_error"):
+              "lse_last_cuda_error", "softmax_lastdim", "log_softmax_dim", "group_norm",
+              "gn_act_residual", "log_softmax_lastdim_host", "gn_act_lse_noalloc"):
         assert n in names, names
 
 
@@ -81,6 +82,25 @@ LSM_ERRORS = [
 def test_log_softmax_validation(lib, args, want):
     assert lib.log_softmax_lastdim(*args, None) == want
     assert lib.log_softmax_lastdim_host(*args, None) == want
+    assert lib.softmax_lastdim(*args, None) == want
+
+
+LSM_DIM_ERRORS = [
+    ((None, None, -1, 3, 3), 2),
+    ((None, None, 2, -3, 3), 2),
+    ((None, None, 2, 3, -3), 2),
+    ((None, None, 2, 0, 3), 0),       # empty reduced axis: no outputs either
+    ((None, None, 2, 3, 3), 1),
+    ((2, 8, 2, 3, 3), 3),
+    ((16, 34, 2, 3, 1), 3),           # inner = 1 goes to the row path, same checks
+    ((None, None, 2**40, 2**40, 2**10), 2),
+    ((None, None, 0, 5, 3), 0),
+]
+
+
+@pytest.mark.parametrize("args,want", LSM_DIM_ERRORS)
+def test_log_softmax_dim_validation(lib, args, want):
+    assert lib.log_softmax_dim(*args, None) == want
 
 
 GN_ERRORS = [
@@ -101,6 +121,8 @@ GN_ERRORS = [
 def test_gn_act_lse_validation(lib, args, want):
     N, C, HW, G, eps = args
     assert lib.gn_act_lse(None, None, None, None, N, C, HW, G, eps, None) == want
+    assert lib.group_norm(None, None, None, None, N, C, HW, G, eps, None) == want
+    assert lib.gn_act_residual(None, None, None, None, N, C, HW, G, eps, None) == want
 
 
 def test_binding_raises_on_error(lib):
