@@ -68,8 +68,8 @@ LAUNCHES = {
     "gn_act_lse": ["gn_fused_kernel"],
     "softmax": ["lsm_ws_kernel"],
     "log_softmax_dim0": ["lse_strided_kernel"],
-    "group_norm": ["gn_fused_kernel"],
-    "gn_act_residual": ["gn_fused_kernel"],
+    "group_norm": ["gn_tma_kernel"],
+    "gn_act_residual": ["gn_tma_kernel"],
 }
 
 
@@ -182,13 +182,22 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha() -> str:
+# The sources that determine each dominant kernel's code (with the shared headers).
+KERNEL_SOURCES = {
+    "lsm_ws_kernel": ["log_softmax.cu"],
+    "lse_strided_kernel": ["lse_strided.cu"],
+    "gn_fused_kernel": ["gn_act_lse.cu", "gn_common.cuh"],
+    "gn_tma_kernel": ["gn_tma.cu", "gn_common.cuh"],
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """sha256 (first 16 hex digits) over the kernel's source files, common.cuh and launch.h."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "log_softmax_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in sorted(KERNEL_SOURCES[kernel] + ["common.cuh", "launch.h"]):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -198,7 +207,7 @@ def ncu_traffic(kernel: str, workload: str):
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(kernel)
     with open(p) as f:
         for line in f:
             line = line.strip()

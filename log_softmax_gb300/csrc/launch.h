@@ -85,6 +85,16 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
                                     int64_t G, float eps, void* scratch, cudaStream_t stream,
                                     int out_kind = 0);
 
+// Form 3 (and GroupNorm alone, and the chain before its lse) on the same
+// work-queue schedule, each item staged through a ring of shared-memory slots
+// by bulk copies.  Applies when HW % 4 == 0, y and out are 16-byte aligned and
+// the ring fits; scratch: gn_tma_scratch_bytes(N, G).  out_kind as above.
+bool gn_tma_applies(const DeviceInfo& dev, const float* y, const float* out, int64_t C, int64_t HW);
+size_t gn_tma_scratch_bytes(int64_t N, int64_t G);
+cudaError_t launch_gn_tma(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
+                          int64_t N, int64_t C, int64_t HW, int64_t G, float eps, void* scratch, cudaStream_t stream,
+                          int out_kind);
+
 // Largest C that the apply kernel's shared-memory table holds.
 constexpr int64_t kGnMaxChannels = 8192;
 

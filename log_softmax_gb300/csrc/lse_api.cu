@@ -242,6 +242,10 @@ lse_status_t check_gn(const float* y, const float* gamma, const float* beta, con
 
 // The one-kernel GroupNorm chain with output kind out_kind (0 channel lse,
 // 1 GroupNorm, 2 chain before the lse), scratch from the device pool.
+// LSE_GN_VARIANT 2 forces the work-queue kernel with per-thread loads, 3 the
+// one with bulk-copy staging (where it applies); by default the elementwise
+// outputs take the bulk-copy kernel and the channel lse the per-thread one
+// (its apply tiles are bound by arithmetic, not by load latency).
 lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, float* out, int64_t N, int64_t C,
                       int64_t HW, int64_t G, float eps, int out_kind, cudaStream_t stream) {
     DeviceState* s = nullptr;
@@ -249,10 +253,17 @@ lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, flo
     if (st != LSE_OK) return st;
     cudaMemPool_t pool = nullptr;
     if ((st = device_pool(s, &pool)) != LSE_OK) return st;
+    const int variant = env_int("LSE_GN_VARIANT", 0);
+    const bool want_tma = variant == 3 || (variant != 2 && out_kind != 0);
+    const bool tma = want_tma && gn_tma_applies(s->info, y, out, C, HW);
     void* scratch = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&scratch, gn_fused_scratch_bytes(N, G), pool, stream);
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, tma ? gn_tma_scratch_bytes(N, G) : gn_fused_scratch_bytes(N, G),
+                                            pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    e = launch_gn_act_lse_fused(s->info, y, gamma, beta, out, N, C, HW, G, eps, scratch, stream, out_kind);
+    if (tma)
+        e = launch_gn_tma(s->info, y, gamma, beta, out, N, C, HW, G, eps, scratch, stream, out_kind);
+    else
+        e = launch_gn_act_lse_fused(s->info, y, gamma, beta, out, N, C, HW, G, eps, scratch, stream, out_kind);
     cudaError_t ef = cudaFreeAsync(scratch, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     if (ef != cudaSuccess) return cuda_fail(ef);
@@ -317,7 +328,7 @@ lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, f
     lse_status_t st = check_gn(y, gamma, beta, out, N, C, HW, G, eps, &empty);
     if (st != LSE_OK || empty) return st;
     // LSE_GN_VARIANT=1 selects the two-kernel path (statistics, then apply);
-    // the default is the one-kernel chain that re-reads each sample from L2.
+    // otherwise one work-queue kernel (see gn_fused).
     if (env_int("LSE_GN_VARIANT", 0) != 1) return gn_fused(y, gamma, beta, out, N, C, HW, G, eps, 0, stream);
     DeviceState* s = nullptr;
     if ((st = device_state(&s)) != LSE_OK) return st;

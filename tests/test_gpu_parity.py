@@ -276,12 +276,18 @@ def test_gn_act_lse_parity(lib, N, C, H, W, G):
 
 GN_CONFIGS = [
     {"LSE_GN_VARIANT": "1"},                                    # statistics kernel + apply kernel
-    {"LSE_GN_VARIANT": "0"},                                    # one kernel, default parts / lag
-    {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "1", "LSE_GN_LAG": "0"},
-    {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "7", "LSE_GN_LAG": "2"},
-    {"LSE_GN_VARIANT": "0", "LSE_GN_PARTS": "16", "LSE_GN_LAG": "100", "LSE_GN_CTAS_PER_SM": "1"},
-    {"LSE_GN_VARIANT": "0", "LSE_GN_THREADS": "512", "LSE_GN_LAG": "3"},
-    {"LSE_GN_VARIANT": "0", "LSE_GN_THREADS": "1024", "LSE_GN_PARTS": "3"},
+    {"LSE_GN_VARIANT": "2"},                                    # work queue, default parts / lag
+    {"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "1", "LSE_GN_LAG": "0"},
+    {"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "7", "LSE_GN_LAG": "2"},
+    {"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "16", "LSE_GN_LAG": "100", "LSE_GN_CTAS_PER_SM": "1"},
+    {"LSE_GN_VARIANT": "2", "LSE_GN_THREADS": "512", "LSE_GN_LAG": "3"},
+    {"LSE_GN_VARIANT": "2", "LSE_GN_THREADS": "1024", "LSE_GN_PARTS": "3"},
+    {"LSE_GN_VARIANT": "0"},                                    # the default choice
+    {"LSE_GN_VARIANT": "3"},                                    # work queue, bulk-copy staging
+    {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "1", "LSE_GNT_LAG": "0"},
+    {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "2", "LSE_GNT_LAG": "2", "LSE_GNT_CTAS_PER_SM": "1"},
+    {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "6", "LSE_GNT_LAG": "100"},
+    {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "8", "LSE_GNT_CTAS_PER_SM": "1"},
 ]
 
 

@@ -218,8 +218,13 @@ def test_gn_elementwise_misaligned(lib, fn):
                   f"{fn} misaligned")
 
 
-@pytest.mark.parametrize("cfg", [{"LSE_GN_PARTS": "5", "LSE_GN_LAG": "0"},
-                                 {"LSE_GN_PARTS": "16", "LSE_GN_LAG": "100", "LSE_GN_CTAS_PER_SM": "1"}])
+@pytest.mark.parametrize("cfg", [{"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "5", "LSE_GN_LAG": "0"},
+                                 {"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "16", "LSE_GN_LAG": "100",
+                                  "LSE_GN_CTAS_PER_SM": "1"},
+                                 {"LSE_GNT_SLOTS": "1", "LSE_GNT_LAG": "0"},
+                                 {"LSE_GNT_SLOTS": "2", "LSE_GNT_LAG": "3", "LSE_GNT_CTAS_PER_SM": "1"},
+                                 {"LSE_GNT_SLOTS": "6", "LSE_GNT_LAG": "100"}],
+                         ids=["queue-p5", "queue-p16", "tma-s1", "tma-s2", "tma-s6"])
 @pytest.mark.parametrize("fn", ["group_norm", "gn_act_residual"])
 def test_gn_elementwise_configs(lib, env, cfg, fn):
     for k, v in cfg.items():
