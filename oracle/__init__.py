@@ -68,9 +68,13 @@ class Oracle:
         lib.oracle_log_softmax_dim.argtypes = [vp, vp, i64, i64, i64]
         for name in ("oracle_group_norm", "oracle_gn_act_residual"):
             getattr(lib, name).argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_double]
+        lib.oracle_conv2d.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64]
+        lib.oracle_conv_gn_act_lse.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                               ctypes.c_double]
         for f in (lib.oracle_lse_reduce, lib.oracle_log_softmax, lib.oracle_row_lse,
                   lib.oracle_gn_act_lse, lib.oracle_softmax, lib.oracle_log_softmax_dim,
-                  lib.oracle_group_norm, lib.oracle_gn_act_residual):
+                  lib.oracle_group_norm, lib.oracle_gn_act_residual, lib.oracle_conv2d,
+                  lib.oracle_conv_gn_act_lse):
             f.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -179,6 +183,33 @@ class Oracle:
         return self._gn_elementwise(self.lib.oracle_gn_act_residual, y, gamma, beta, G, eps)
 
 
+    def conv2d(self, x, w, b) -> np.ndarray:
+        """Valid stride-1 Conv2d with bias: x [N, Cin, H, W], w [Cout, Cin, KH, KW], b [Cout]."""
+        x, w, b = _f32(x), _f32(w), _f32(b)
+        N, Cin, H, W = x.shape
+        Cout, Cin2, KH, KW = w.shape
+        assert Cin2 == Cin and b.size == Cout
+        out = np.empty((N, Cout, H - KH + 1, W - KW + 1), dtype=np.float64)
+        rc = self.lib.oracle_conv2d(_p(x), _p(w), _p(b), _p(out), N, Cin, H, W, Cout, KH, KW)
+        if rc != 0:
+            raise ValueError(f"oracle_conv2d rejected its arguments (rc={rc})")
+        return out
+
+    def conv_gn_act_lse(self, x, w, b, gamma, beta, G: int, eps: float = 1e-5) -> np.ndarray:
+        """Conv2d 3x3 (valid, bias) -> GroupNorm -> tanh -> hardswish -> +y -> channel
+        logsumexp (keepdim): [N, 1, H - 2, W - 2]."""
+        x, w, b, gamma, beta = _f32(x), _f32(w), _f32(b), _f32(gamma), _f32(beta)
+        N, Cin, H, W = x.shape
+        Cout = w.shape[0]
+        assert w.shape == (Cout, Cin, 3, 3) and b.size == Cout and gamma.size == Cout and beta.size == Cout
+        out = np.empty((N, 1, H - 2, W - 2), dtype=np.float64)
+        rc = self.lib.oracle_conv_gn_act_lse(_p(x), _p(w), _p(b), _p(gamma), _p(beta), _p(out), N, Cin,
+                                             H, W, Cout, G, float(np.float32(eps)))
+        if rc != 0:
+            raise ValueError(f"oracle_conv_gn_act_lse rejected its arguments (rc={rc})")
+        return out
+
+
 def default() -> Oracle:
     """The committed oracle, compiled on first use."""
     global _default
@@ -222,3 +253,11 @@ def group_norm(y, gamma, beta, G: int, eps: float = 1e-5) -> np.ndarray:
 
 def gn_act_residual(y, gamma, beta, G: int, eps: float = 1e-5) -> np.ndarray:
     return default().gn_act_residual(y, gamma, beta, G, eps)
+
+
+def conv2d(x, w, b) -> np.ndarray:
+    return default().conv2d(x, w, b)
+
+
+def conv_gn_act_lse(x, w, b, gamma, beta, G: int, eps: float = 1e-5) -> np.ndarray:
+    return default().conv_gn_act_lse(x, w, b, gamma, beta, G, eps)

@@ -23,7 +23,9 @@
  *       per (sample, group) mean and population variance (unbiased=False) over
  *       the group's C/G channels and all H*W positions, normalised as
  *       (x - mean) / sqrt(var + eps), then the per-channel affine weight and
- *       bias; HardSwish(t) = t * min(max(t + 3, 0), 6) / 6.
+ *       bias; HardSwish(t) = t * min(max(t + 3, 0), 6) / 6.  The chain's input
+ *       is a Conv2d with 8 input and 64 output channels, kernel 3, stride 1,
+ *       no padding (128 x 128 input planes give 126 x 126 outputs), with bias.
  *
  * Special values (the pages are silent; the readings taken here):
  *  - a NaN anywhere in the reduced set gives NaN;
@@ -244,4 +246,76 @@ int oracle_gn_act_residual(const float* y, const float* gamma, const float* beta
                            int64_t N, int64_t C, int64_t HW, int64_t G, double eps)
 {
     return group_norm_impl(y, gamma, beta, out, N, C, HW, G, eps, 1);
+}
+
+/* [P3] Conv2d as the chain's first layer: valid cross-correlation, stride 1,
+ * no padding, with bias.  x is [N, Cin, H, W], w is [Cout, Cin, KH, KW], b is
+ * [Cout]; y is [N, Cout, H - KH + 1, W - KW + 1]:
+ *   y[n,co,i,j] = b[co] + sum over ci, u, v of w[co,ci,u,v] * x[n,ci,i+u,j+v]
+ * accumulated in double. */
+int oracle_conv2d(const float* x, const float* w, const float* b, double* y, int64_t N, int64_t Cin,
+                  int64_t H, int64_t W, int64_t Cout, int64_t KH, int64_t KW)
+{
+    if (!x || !w || !b || !y || N < 0 || Cin <= 0 || Cout <= 0 || KH <= 0 || KW <= 0 || H < KH || W < KW)
+        return -1;
+    const int64_t OH = H - KH + 1, OW = W - KW + 1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t co = 0; co < Cout; ++co)
+            for (int64_t i = 0; i < OH; ++i)
+                for (int64_t j = 0; j < OW; ++j) {
+                    double acc = (double)b[co];
+                    for (int64_t ci = 0; ci < Cin; ++ci)
+                        for (int64_t u = 0; u < KH; ++u)
+                            for (int64_t v = 0; v < KW; ++v)
+                                acc += (double)w[((co * Cin + ci) * KH + u) * KW + v] *
+                                       (double)x[((n * Cin + ci) * H + i + u) * W + j + v];
+                    y[((n * Cout + co) * OH + i) * OW + j] = acc;
+                }
+    return 0;
+}
+
+/* [P3] the whole chain from the convolution's input: y = Conv2d(x) (3 x 3,
+ * valid, bias) kept in double, then the GroupNorm -> tanh -> hardswish ->
+ * residual -> channel logsumexp steps of oracle_gn_act_lse on that y.
+ * out is [N, OH * OW]. */
+int oracle_conv_gn_act_lse(const float* x, const float* w, const float* b, const float* gamma,
+                           const float* beta, double* out, int64_t N, int64_t Cin, int64_t H,
+                           int64_t W, int64_t Cout, int64_t G, double eps)
+{
+    if (!gamma || !beta || !out || G <= 0 || Cout % G != 0 || H < 3 || W < 3) return -1;
+    const int64_t OH = H - 2, OW = W - 2, HW = OH * OW, C = Cout, cpg = C / G;
+    double* y = (double*)malloc(sizeof(double) * (size_t)(N * C * HW > 0 ? N * C * HW : 1));
+    double* r = (double*)malloc(sizeof(double) * (size_t)C);
+    double* mean = (double*)malloc(sizeof(double) * (size_t)G);
+    double* rstd = (double*)malloc(sizeof(double) * (size_t)G);
+    if (!y || !r || !mean || !rstd) { free(y); free(r); free(mean); free(rstd); return -2; }
+    int rc = oracle_conv2d(x, w, b, y, N, Cin, H, W, Cout, 3, 3);
+    for (int64_t n = 0; rc == 0 && n < N; ++n) {
+        const double* yn = y + n * C * HW;
+        for (int64_t g = 0; g < G; ++g) {
+            const double* span = yn + g * cpg * HW;
+            const int64_t count = cpg * HW;
+            double sum = 0.0;
+            for (int64_t k = 0; k < count; ++k) sum += span[k];
+            const double mu = sum / (double)count;
+            double sq = 0.0;
+            for (int64_t k = 0; k < count; ++k) sq += (span[k] - mu) * (span[k] - mu);
+            mean[g] = mu;
+            rstd[g] = 1.0 / sqrt(sq / (double)count + eps);
+        }
+        for (int64_t p = 0; p < HW; ++p) {
+            for (int64_t c = 0; c < C; ++c) {
+                const int64_t g = c / cpg;
+                const double v = yn[c * HW + p];
+                const double z = (v - mean[g]) * rstd[g] * (double)gamma[c] + (double)beta[c];
+                r[c] = v + hardswish(tanh(z));
+            }
+            out[n * HW + p] = lse_strided_double(r, C, 1);
+        }
+    }
+    free(y);
+    free(r);
+    free(mean);
+    free(rstd);
+    return rc;
 }

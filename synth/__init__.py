@@ -54,7 +54,8 @@ class Workload:
     """A named workload: what is computed, on which shape, from which recipe."""
     name: str
     op: str                      # "lse_dim0" | "log_softmax" | "gn_act_lse" | "softmax" |
-                                 # "log_softmax_dim0" | "group_norm" | "gn_act_residual"
+                                 # "log_softmax_dim0" | "group_norm" | "gn_act_residual" |
+                                 # "conv_gn_act_lse"
     shape: tuple
     recipe: str
     params: dict = field(default_factory=dict)
@@ -101,6 +102,16 @@ for _name, _op, _like in (
     _w = WORKLOADS[_like]
     WORKLOADS[_name] = Workload(_name, _op, _w.shape, _w.recipe, dict(_w.params, like=_like))
 
+# The chain from its convolution's input: x [128, 8, 128, 128] through Conv2d(8 -> 64, 3 x 3,
+# valid, bias) to the y of the chain above.  The weights are drawn like a freshly
+# initialised layer (uniform within +-1/sqrt(fan_in), fan_in = 8 * 3 * 3).
+WORKLOADS["conv_gn_act_lse_128x8x128x128"] = Workload(
+    "conv_gn_act_lse_128x8x128x128", "conv_gn_act_lse", (128, 8, 128, 128),
+    "x ~ N(0,1) seed 6; w [64,8,3,3] and bias [64] ~ U[-1/sqrt(72), 1/sqrt(72)) seeds 106, 206; "
+    "gamma ~ U[0.5,1.5) seed 105; beta ~ N(0,0.1) seed 205; G=16, eps=1e-5",
+    {"seed": 6, "w_seed": 106, "bias_seed": 206, "gamma_seed": 105, "beta_seed": 205, "Cout": 64,
+     "G": 16, "eps": 1e-5})
+
 
 def make_inputs(w: Workload | str, device="cpu", shape=None):
     """Draw the inputs of a workload (optionally at another shape, same recipe).
@@ -127,6 +138,16 @@ def make_inputs(w: Workload | str, device="cpu", shape=None):
         return {"x": uniform(shape, p["seed"], -20.0, 20.0, device=device)}
     if base == "log_softmax_4096x393216":
         return {"x": normal(shape, p["seed"], device=device)}
+    if base == "conv_gn_act_lse_128x8x128x128":
+        Cin, Cout = shape[1], p["Cout"]
+        bound = 1.0 / math.sqrt(Cin * 9)
+        return {
+            "x": normal(shape, p["seed"], device=device),
+            "w": uniform((Cout, Cin, 3, 3), p["w_seed"], -bound, bound, device=device),
+            "bias": uniform((Cout,), p["bias_seed"], -bound, bound, device=device),
+            "gamma": uniform((Cout,), p["gamma_seed"], 0.5, 1.5, device=device),
+            "beta": normal((Cout,), p["beta_seed"], var=0.1, device=device),
+        }
     if base == "gn_act_lse_128x64x126x126":
         C = shape[1]
         return {

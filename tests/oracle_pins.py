@@ -346,6 +346,65 @@ def pin_gn_act_residual_torch(orc):
     _close(orc.gn_act_residual(y, gamma, beta, G, 1e-5), ref, rtol=1e-12, atol=1e-12)
 
 
+# --------------------------------------------------------------------- Conv2d and the conv-fed chain
+
+def pin_conv_torch(orc):
+    """Valid stride-1 Conv2d with bias agrees with float64 torch.nn.functional.conv2d
+    (non-square planes, Cin != Cout, a non-square kernel)."""
+    rng = _rng(61)
+    x = rng.normal(0, 1, size=(2, 3, 6, 9)).astype(np.float32)
+    w = rng.uniform(-0.5, 0.5, size=(5, 3, 3, 2)).astype(np.float32)
+    b = rng.normal(0, 1, size=5).astype(np.float32)
+    ref = F.conv2d(torch.from_numpy(x).double(), torch.from_numpy(w).double(),
+                   torch.from_numpy(b).double()).numpy()
+    _close(orc.conv2d(x, w, b), ref, rtol=1e-13, atol=1e-13)
+
+
+def pin_conv_delta(orc):
+    """A weight that is 1 at (co, ci, u, v) and 0 elsewhere copies channel ci shifted by
+    (u, v) into channel co: y[n, co, i, j] = x[n, ci, i + u, j + v] + b[co]; no other
+    channel receives anything but its bias.  Fixes the index order of every operand."""
+    rng = _rng(62)
+    x = rng.normal(0, 1, size=(2, 3, 5, 7)).astype(np.float32)
+    for co, ci, u, v in ((0, 2, 0, 1), (3, 0, 2, 0), (1, 1, 1, 2)):
+        w = np.zeros((4, 3, 3, 3), dtype=np.float32)
+        w[co, ci, u, v] = 1.0
+        b = np.arange(4, dtype=np.float32) * 0.25
+        y = orc.conv2d(x, w, b)
+        exp = np.broadcast_to(b.astype(np.float64)[None, :, None, None], y.shape).copy()
+        exp[:, co] += x[:, ci, u:u + 3, v:v + 5].astype(np.float64)
+        _close(y, exp, rtol=0, atol=0)
+
+
+def pin_conv_constant(orc):
+    """Constant input c gives b[co] + c * sum of w[co] at every output pixel."""
+    rng = _rng(63)
+    w = rng.uniform(-1, 1, size=(4, 2, 3, 3)).astype(np.float32)
+    b = rng.normal(0, 1, size=4).astype(np.float32)
+    c = 1.75
+    x = np.full((1, 2, 4, 6), c, dtype=np.float32)
+    y = orc.conv2d(x, w, b)
+    exp = b.astype(np.float64) + c * w.astype(np.float64).reshape(4, -1).sum(1)
+    _close(y, np.broadcast_to(exp[None, :, None, None], y.shape), rtol=1e-14, atol=1e-14)
+
+
+def pin_conv_chain_torch(orc):
+    """Conv2d -> GroupNorm -> tanh -> hardswish -> + conv output -> logsumexp over channels,
+    keepdim, agrees with the float64 torch composition of the same layers."""
+    rng = _rng(64)
+    N, Cin, H, W, Cout, G = 2, 3, 7, 6, 8, 4
+    x = rng.normal(0, 1, size=(N, Cin, H, W)).astype(np.float32)
+    w = rng.uniform(-0.3, 0.3, size=(Cout, Cin, 3, 3)).astype(np.float32)
+    b = rng.uniform(-0.3, 0.3, size=Cout).astype(np.float32)
+    gamma = rng.uniform(0.5, 1.5, size=Cout).astype(np.float32)
+    beta = rng.normal(0, 0.3, size=Cout).astype(np.float32)
+    y = F.conv2d(torch.from_numpy(x).double(), torch.from_numpy(w).double(), torch.from_numpy(b).double())
+    z = F.group_norm(y, G, torch.from_numpy(gamma).double(), torch.from_numpy(beta).double(),
+                     eps=float(np.float32(1e-5)))
+    ref = torch.logsumexp(y + F.hardswish(torch.tanh(z)), dim=1, keepdim=True).numpy()
+    _close(orc.conv_gn_act_lse(x, w, b, gamma, beta, G, 1e-5), ref, rtol=1e-12, atol=1e-12)
+
+
 # --------------------------------------------------------------------- stored closed forms
 
 def pin_golden_closed_forms(orc):

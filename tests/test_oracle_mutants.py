@@ -46,6 +46,14 @@ MUTANTS = [
     ("chain_no_residual", "act ? v + hardswish(tanh(z)) : z", "act ? hardswish(tanh(z)) : z", 0),
     ("groupnorm_affine_swapped", "(v - mu) * rs * (double)gamma[c] + (double)beta[c]",
      "(v - mu) * rs * (double)beta[c] + (double)gamma[c]", 0),
+    ("conv_no_bias", "double acc = (double)b[co];", "double acc = 0.0;", 0),
+    ("conv_taps_transposed", "x[((n * Cin + ci) * H + i + u) * W + j + v]",
+     "x[((n * Cin + ci) * H + i + v) * W + j + u]", 0),
+    ("conv_kernel_flipped", "w[((co * Cin + ci) * KH + u) * KW + v]",
+     "w[((co * Cin + ci) * KH + (KH - 1 - u)) * KW + (KW - 1 - v)]", 0),
+    ("conv_chain_unbiased", "rstd[g] = 1.0 / sqrt(sq / (double)count + eps);",
+     "rstd[g] = 1.0 / sqrt(sq / (double)(count - 1) + eps);", 0),
+    ("conv_chain_no_residual", "r[c] = v + hardswish(tanh(z));", "r[c] = hardswish(tanh(z));", 1),
 ]
 
 
