@@ -56,6 +56,13 @@ def algorithmic_bytes(w: synth.Workload) -> int:
     if w.op in GN_ELEMENTWISE:
         C = w.shape[1]
         return 4 * (2 * w.numel + 2 * C)
+    if w.op == "conv_gn_act_lse":
+        # x once, y written once by the conv and read once by the apply pass, out;
+        # weights, bias, gamma, beta
+        N, Cin, H, W = w.shape
+        Cout = w.params["Cout"]
+        ohw = (H - 2) * (W - 2)
+        return 4 * (w.numel + 2 * N * Cout * ohw + N * ohw + Cout * (Cin * 9 + 3))
     raise KeyError(w.op)
 
 
@@ -70,6 +77,7 @@ LAUNCHES = {
     "log_softmax_dim0": ["lse_strided_kernel"],
     "group_norm": ["gn_tma_kernel"],
     "gn_act_residual": ["gn_tma_kernel"],
+    "conv_gn_act_lse": ["conv2d_tc_kernel", "gn_tile_merge_kernel", "gn_apply_kernel"],
 }
 
 
@@ -89,6 +97,11 @@ def make_step(L, w: synth.Workload, inputs, out, stream):
         inner = w.numel // R
         x = inputs["x"]
         return lambda: L.log_softmax_dim(x, out, 1, R, inner, stream=stream)
+    if w.op == "conv_gn_act_lse":
+        N, Cin, H, W = w.shape
+        x, wt, b, g, be = (inputs[k] for k in ("x", "w", "bias", "gamma", "beta"))
+        G, eps, Cout = w.params["G"], w.params["eps"], w.params["Cout"]
+        return lambda: L.conv_gn_act_lse(x, wt, b, g, be, out, N, Cin, H, W, Cout, G, eps, stream=stream)
     if w.op == "gn_act_lse" or w.op in GN_ELEMENTWISE:
         N, C, H, W = w.shape
         y, g, b = inputs["y"], inputs["gamma"], inputs["beta"]
@@ -104,6 +117,9 @@ def out_shape(w: synth.Workload):
     if w.op == "gn_act_lse":
         N, C, H, W = w.shape
         return (N, 1, H, W)
+    if w.op == "conv_gn_act_lse":
+        N, Cin, H, W = w.shape
+        return (N, 1, H - 2, W - 2)
     return w.shape
 
 
@@ -122,6 +138,14 @@ def oracle_call(w: synth.Workload, inputs) -> int:
             return 4 * (x.numel() + x.shape[1])
         oracle.log_softmax_dim(x, 1, x.shape[0], x.shape[1])
         return 8 * x.numel()
+    if w.op == "conv_gn_act_lse":
+        x = inputs["x"]
+        oracle.conv_gn_act_lse(x, inputs["w"], inputs["bias"], inputs["gamma"], inputs["beta"], w.params["G"],
+                               w.params["eps"])
+        N, Cin, H, W = x.shape
+        Cout = w.params["Cout"]
+        ohw = (H - 2) * (W - 2)
+        return 4 * (x.numel() + 2 * N * Cout * ohw + N * ohw)
     y, g, b = inputs["y"], inputs["gamma"], inputs["beta"]
     getattr(oracle, w.op)(y, g, b, w.params["G"], w.params["eps"])
     if w.op == "gn_act_lse":
@@ -188,6 +212,7 @@ KERNEL_SOURCES = {
     "lse_strided_kernel": ["lse_strided.cu"],
     "gn_fused_kernel": ["gn_act_lse.cu", "gn_common.cuh"],
     "gn_tma_kernel": ["gn_tma.cu", "gn_common.cuh"],
+    "conv2d_tc_kernel": ["conv.cu", "conv_tile.cuh", "gn_common.cuh"],
 }
 
 
@@ -301,7 +326,7 @@ def time_oracle(w: synth.Workload, sample, budget_s: float, unit: int):
     if w.op in ("lse_dim0", "log_softmax_dim0"):
         n_units = sample["x"].shape[1] // unit
     else:
-        n_units = next(iter(sample.values())).shape[0] // unit
+        n_units = sample["x" if "x" in sample else "y"].shape[0] // unit
     n_units = max(1, n_units)
     t0 = time.perf_counter()
     done_bytes = 0
@@ -310,6 +335,8 @@ def time_oracle(w: synth.Workload, sample, budget_s: float, unit: int):
         k = units % n_units
         if w.op in ("lse_dim0", "log_softmax_dim0"):
             sl = {"x": sample["x"][:, k * unit:(k + 1) * unit].contiguous()}
+        elif w.op == "conv_gn_act_lse":
+            sl = dict(sample, x=sample["x"][k * unit:(k + 1) * unit])
         elif "x" in sample:
             sl = {"x": sample["x"][k * unit:(k + 1) * unit]}
         else:
@@ -331,6 +358,10 @@ def oracle_sample(w: synth.Workload, inputs_dev, rows: int):
         inner = w.numel // R
         cols = min(inner, rows * 4096)
         return {"x": inputs_dev["x"].view(R, inner)[:, :cols].cpu().contiguous()}, 4096
+    if w.op == "conv_gn_act_lse":
+        smp = {k: v.cpu().contiguous() for k, v in inputs_dev.items() if k != "x"}
+        smp["x"] = inputs_dev["x"][:max(1, rows // 64)].cpu().contiguous()
+        return smp, 1
     y = inputs_dev["y"][:max(1, rows // 64)].cpu().contiguous()
     return {"y": y, "gamma": inputs_dev["gamma"].cpu(), "beta": inputs_dev["beta"].cpu()}, 1
 
@@ -341,7 +372,8 @@ def sample_text(w: synth.Workload, sample, units: int) -> str:
     if w.op in ("lse_dim0", "log_softmax_dim0"):
         return (f"{units} passes of R={w.shape[0]} x 4096 columns over the first "
                 f"{sample['x'].shape[1]} columns")
-    return (f"{units} sample passes over the first {sample['y'].shape[0]} samples of "
+    key = "x" if w.op == "conv_gn_act_lse" else "y"
+    return (f"{units} sample passes over the first {sample[key].shape[0]} samples of "
             f"{list(w.shape[1:])}")
 
 
@@ -538,6 +570,9 @@ def run_e2e(L, w: synth.Workload, inputs, args, dev, world):
             L.logsumexp(host_in["x"], dim=0, out=host_out)
         elif w.op == "log_softmax_dim0":
             L.log_softmax(host_in["x"], out=host_out, dim=0)
+        elif w.op == "conv_gn_act_lse":
+            L.conv_gn_act_lse_forward(*(host_in[k] for k in ("x", "w", "bias", "gamma", "beta")), w.params["G"],
+                                      w.params["eps"], out=host_out)
         else:
             fn = {"gn_act_lse": L.gn_act_lse_forward, "group_norm": L.group_norm_forward,
                   "gn_act_residual": L.gn_act_residual_forward}[w.op]

@@ -161,6 +161,41 @@ lse_status_t gn_act_residual(const float* y, const float* gamma, const float* be
                              cudaStream_t stream);
 
 /*
+ * conv2d_3x3 — the Conv2d that produces the chain's input in "Kimi-K2.6 / l2_p92"
+ * (its model: Conv2d(8, 64, kernel_size=3), stride 1, no padding, with bias):
+ *   y[n,co,i,j] = b[co] + sum over ci, u, v of w[co,ci,u,v] * x[n,ci,i+u,j+v]
+ *   x  [N * Cin * H * W] fp32 NCHW, device, read only.
+ *   w  [Cout * Cin * 3 * 3] fp32, device, read only;  b [Cout] fp32, device.
+ *   y  [N * Cout * (H-2) * (W-2)] fp32, device, written (must not alias x).
+ *   N >= 0, H >= 3, W >= 3; 1 <= Cin <= 8 and Cout a multiple of 16 up to 128
+ *   (else LSE_ERR_UNSUPPORTED).
+ * Computed on the tensor cores as an implicit GEMM per 128-pixel tile with
+ * every operand split into two tf32 parts (three products per pair), which
+ * keeps fp32 accuracy: |err| <= 2e-5 + 1e-6 * |ref| against a double
+ * evaluation for data of unit scale.
+ */
+lse_status_t conv2d_3x3(const float* x, const float* w, const float* b, float* y, int64_t N, int64_t Cin,
+                        int64_t H, int64_t W, int64_t Cout, cudaStream_t stream);
+
+/*
+ * conv_gn_act_lse — the whole chain of "Kimi-K2.6 / l2_p92" from the
+ * convolution's input: y = conv2d_3x3(x, w, b), then gn_act_lse(y, ...):
+ *   out[n,p] = lse over c of ( y + hardswish(tanh(GroupNorm(y))) )[n,c,p]
+ *   x, w, b as conv2d_3x3; gamma, beta [Cout]; out [N * (H-2) * (W-2)] fp32,
+ *   device, written.  Cin = 8 (the page's layer), Cout % G == 0 with Cout / G
+ *   in {1, 2, 4, 8, 16} and G <= 64 (else LSE_ERR_UNSUPPORTED); eps >= 0 and
+ *   finite; the
+ *   conv2d_3x3 shape rules.  Other shapes: conv2d_3x3 then gn_act_lse.
+ * The convolution's epilogue writes y and the Welford partials of every
+ * (sample, 128-pixel tile, group), so the statistics never re-read y; the
+ * apply pass reads y once.  Scratch (y itself, about N*Cout*(H-2)*(W-2)*4
+ * bytes, plus the partials) comes from the library's pool on `stream`.
+ */
+lse_status_t conv_gn_act_lse(const float* x, const float* w, const float* b, const float* gamma,
+                             const float* beta, float* out, int64_t N, int64_t Cin, int64_t H, int64_t W,
+                             int64_t Cout, int64_t G, float eps, cudaStream_t stream);
+
+/*
  * gn_act_lse — GroupNorm -> tanh -> hardswish -> residual add -> logsumexp over
  * channels, keepdim ("Kimi-K2.6 / l2_p92", the chain after its Conv2d):
  *   mean[n,g], var[n,g] : population statistics of the C/G channels of group g

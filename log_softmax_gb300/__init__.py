@@ -15,10 +15,13 @@ C-ABI entry points (declared in include/lse.h), same names here:
     gn_act_lse_noalloc(y, gamma, beta, out, N, C, HW, G, eps, stream=None)
     group_norm(y, gamma, beta, out, N, C, HW, G, eps, stream=None)
     gn_act_residual(y, gamma, beta, out, N, C, HW, G, eps, stream=None)
+    conv2d_3x3(x, w, b, y, N, Cin, H, W, Cout, stream=None)
+    conv_gn_act_lse(x, w, b, gamma, beta, out, N, Cin, H, W, Cout, G, eps, stream=None)
 Conveniences that allocate the output with torch:
     logsumexp(x, dim=0), log_softmax(x, dim=-1), softmax(x),
     gn_act_lse_forward(y, gamma, beta, G, eps), group_norm_forward(...),
-    gn_act_residual_forward(...)
+    gn_act_residual_forward(...), conv2d_3x3_forward(x, w, b),
+    conv_gn_act_lse_forward(x, w, b, gamma, beta, G, eps)
 """
 from __future__ import annotations
 
@@ -38,6 +41,7 @@ STATUS = {
 
 EXPORTS = ("lse_reduce", "log_softmax_lastdim", "log_softmax_lastdim_host", "softmax_lastdim",
            "log_softmax_dim", "gn_act_lse", "gn_act_lse_noalloc", "group_norm", "gn_act_residual",
+           "conv2d_3x3", "conv_gn_act_lse",
            "lse_release_workspace", "lse_device_status", "lse_status_string", "lse_last_cuda_error",
            "lse_version")
 
@@ -70,6 +74,8 @@ def load_library(path: str = LIB_PATH):
     lib.softmax_lastdim.argtypes = [vp, vp, i64, i64, vp]
     lib.log_softmax_dim.argtypes = [vp, vp, i64, i64, i64, vp]
     lib.gn_act_lse.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
+    lib.conv2d_3x3.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp]
+    lib.conv_gn_act_lse.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp]
     lib.group_norm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
     lib.gn_act_residual.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
     lib.gn_act_lse_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, vp]
@@ -81,7 +87,8 @@ def load_library(path: str = LIB_PATH):
     lib.lse_last_cuda_error.argtypes = []
     lib.lse_version.argtypes = []
     for name in ("lse_reduce", "log_softmax_lastdim", "softmax_lastdim", "log_softmax_dim",
-                 "gn_act_lse", "group_norm", "gn_act_residual", "lse_release_workspace",
+                 "gn_act_lse", "group_norm", "gn_act_residual", "conv2d_3x3", "conv_gn_act_lse",
+                 "lse_release_workspace",
                  "lse_device_status", "lse_last_cuda_error", "lse_version"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -211,6 +218,26 @@ def gn_act_residual(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: f
         rc = lib.gn_act_residual(_ptr(y), _ptr(gamma), _ptr(beta), _ptr(out), int(N), int(C),
                                  int(HW), int(G), float(eps), _stream(stream, y))
     _check("gn_act_residual", rc)
+
+
+def conv2d_3x3(x, w, b, y, N: int, Cin: int, H: int, W: int, Cout: int, stream=None) -> None:
+    """Conv2d 3x3, stride 1, no padding, with bias: x [N,Cin,H,W] -> y [N,Cout,H-2,W-2]."""
+    lib = load_library()
+    with _device_of(x):
+        rc = lib.conv2d_3x3(_ptr(x), _ptr(w), _ptr(b), _ptr(y), int(N), int(Cin), int(H), int(W), int(Cout),
+                            _stream(stream, x))
+    _check("conv2d_3x3", rc)
+
+
+def conv_gn_act_lse(x, w, b, gamma, beta, out, N: int, Cin: int, H: int, W: int, Cout: int, G: int,
+                    eps: float, stream=None) -> None:
+    """Conv2d 3x3 (valid, bias) -> GroupNorm -> tanh -> hardswish -> + conv output ->
+    logsumexp over channels; out is [N, H-2, W-2]."""
+    lib = load_library()
+    with _device_of(x):
+        rc = lib.conv_gn_act_lse(_ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(out), int(N), int(Cin),
+                                 int(H), int(W), int(Cout), int(G), float(eps), _stream(stream, x))
+    _check("conv_gn_act_lse", rc)
 
 
 def gn_act_lse_noalloc(y, gamma, beta, out, N: int, C: int, HW: int, G: int, eps: float,
@@ -370,6 +397,31 @@ def gn_act_residual_forward(y: torch.Tensor, gamma: torch.Tensor, beta: torch.Te
                             eps: float = 1e-5, out=None, device="cuda") -> torch.Tensor:
     """y + hardswish(tanh(GroupNorm(y))) for y [N, C, *spatial]; same shape out."""
     return _gn_call(gn_act_residual, y, gamma, beta, G, eps, out, device)
+
+
+def conv2d_3x3_forward(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor, out=None,
+                       device="cuda") -> torch.Tensor:
+    """Conv2d(Cin, Cout, 3) (stride 1, no padding, bias) of x [N, Cin, H, W]."""
+    xd, host = _to_device(x, device)
+    wd, _ = _to_device(w, xd.device)
+    bd, _ = _to_device(b, xd.device)
+    N, Cin, H, W = xd.shape
+    Cout = wd.shape[0]
+    res = _device_out((N, Cout, H - 2, W - 2), xd, host, out)
+    conv2d_3x3(xd, wd, bd, res, N, Cin, H, W, Cout)
+    return _result(res, host, out)
+
+
+def conv_gn_act_lse_forward(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor, gamma: torch.Tensor,
+                            beta: torch.Tensor, G: int, eps: float = 1e-5, out=None,
+                            device="cuda") -> torch.Tensor:
+    """The chain from the convolution's input x [N, Cin, H, W]; returns [N, 1, H-2, W-2]."""
+    xd, host = _to_device(x, device)
+    wd, bd, gd, betad = (_to_device(t, xd.device)[0] for t in (w, b, gamma, beta))
+    N, Cin, H, W = xd.shape
+    res = _device_out((N, 1, H - 2, W - 2), xd, host, out)
+    conv_gn_act_lse(xd, wd, bd, gd, betad, res, N, Cin, H, W, wd.shape[0], G, eps)
+    return _result(res, host, out)
 
 
 def gn_act_lse_forward(y: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, G: int,

@@ -373,9 +373,7 @@ cudaError_t launch_gn_act_lse(const DeviceInfo& dev, const float* y, const float
                               const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
                               int64_t G, float eps, float* stats, cudaStream_t stream) {
     const bool y16 = (reinterpret_cast<uintptr_t>(y) & 15) == 0;
-    const bool o16 = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
     const bool vec_stats = (HW % 4 == 0) && y16;
-    const bool vec_apply = (HW % 4 == 0) && y16 && o16;
     {
         const int64_t ngrp = N * G;
         const int64_t cap = (int64_t)dev.sm_count * 4 * 16;
@@ -387,6 +385,13 @@ cudaError_t launch_gn_act_lse(const DeviceInfo& dev, const float* y, const float
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    return launch_gn_apply(dev, y, gamma, beta, out, N, C, HW, G, stats, stream);
+}
+
+cudaError_t launch_gn_apply(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
+                            int64_t N, int64_t C, int64_t HW, int64_t G, const float* stats, cudaStream_t stream) {
+    const bool vec_apply = (HW % 4 == 0) && (reinterpret_cast<uintptr_t>(y) & 15) == 0 &&
+                           (reinterpret_cast<uintptr_t>(out) & 15) == 0;
     {
         const int VEC = vec_apply ? 4 : 1;
         const int64_t tiles = ((HW + VEC - 1) / VEC + 127) / 128;

@@ -74,6 +74,11 @@ cudaError_t launch_gn_act_lse(const DeviceInfo& dev, const float* y, const float
                               const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
                               int64_t G, float eps, float* stats, cudaStream_t stream);
 
+// The apply stage alone: per-(n, g) stats (mean, 1/sqrt(var + eps)) in, the
+// normalise / tanh / hardswish / residual / channel-lse pass out.
+cudaError_t launch_gn_apply(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
+                            int64_t N, int64_t C, int64_t HW, int64_t G, const float* stats, cudaStream_t stream);
+
 // Form 3 in one cooperative kernel: statistics parts and apply tiles of the
 // samples claimed from one work queue, each sample's second read close behind
 // its first so that it hits L2.  Scratch: gn_fused_scratch_bytes(N, G).
@@ -94,6 +99,23 @@ size_t gn_tma_scratch_bytes(int64_t N, int64_t G);
 cudaError_t launch_gn_tma(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
                           int64_t N, int64_t C, int64_t HW, int64_t G, float eps, void* scratch, cudaStream_t stream,
                           int out_kind);
+
+// Conv2d 3 x 3, stride 1, valid, with bias, on the tensor cores (3xTF32):
+// x [N, cin, H, W] -> y [N, cout, H - 2, W - 2].  Shapes conv_tc_supported()
+// accepts: 1 <= cin <= 8, cout a multiple of 16 up to 128.
+bool conv_tc_supported(int64_t cin, int64_t cout);
+cudaError_t launch_conv2d_3x3(const DeviceInfo& dev, const float* x, const float* w, const float* b, float* y,
+                              int64_t N, int64_t cin, int64_t H, int64_t W, int64_t cout, cudaStream_t stream);
+
+// The chain from the convolution's input: the conv kernel writes y and, per
+// 128-pixel tile, the Welford partial of each of the G channel groups; a merge
+// kernel reduces them to per-(n, g) stats; launch_gn_apply finishes.  Scratch:
+// conv_chain_scratch_bytes(...), y included.
+size_t conv_chain_scratch_bytes(int64_t N, int64_t H, int64_t W, int64_t cout, int64_t G);
+cudaError_t launch_conv_gn_act_lse(const DeviceInfo& dev, const float* x, const float* w, const float* b,
+                                   const float* gamma, const float* beta, float* out, int64_t N, int64_t cin,
+                                   int64_t H, int64_t W, int64_t cout, int64_t G, float eps, void* scratch,
+                                   cudaStream_t stream);
 
 // Largest C that the apply kernel's shared-memory table holds.
 constexpr int64_t kGnMaxChannels = 8192;

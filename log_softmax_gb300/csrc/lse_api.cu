@@ -305,6 +305,57 @@ lse_status_t log_softmax_dim(const float* x, float* out, int64_t outer, int64_t 
     return e == cudaSuccess ? LSE_OK : cuda_fail(e);
 }
 
+lse_status_t conv2d_3x3(const float* x, const float* w, const float* b, float* y, int64_t N, int64_t Cin,
+                        int64_t H, int64_t W, int64_t Cout, cudaStream_t stream) {
+    if (N < 0 || Cin <= 0 || Cout <= 0 || H < 3 || W < 3) return LSE_ERR_SIZE;
+    int64_t nin = 0, nout = 0;
+    if (!mul_ok(N, Cin, &nin) || !mul_ok(nin, H, &nin) || !mul_ok(nin, W, &nin) || nin > INT64_MAX / 4 ||
+        !mul_ok(N, Cout, &nout) || !mul_ok(nout, (H - 2) * (W - 2), &nout) || nout > INT64_MAX / 4 ||
+        H > INT32_MAX || W > INT32_MAX)
+        return LSE_ERR_SIZE;
+    if (!conv_tc_supported(Cin, Cout)) return LSE_ERR_UNSUPPORTED;
+    if (nout == 0) return LSE_OK;
+    if (!x || !w || !b || !y) return LSE_ERR_NULL;
+    if (!aligned4(x) || !aligned4(w) || !aligned4(b) || !aligned4(y)) return LSE_ERR_ALIGN;
+    DeviceState* s = nullptr;
+    lse_status_t st = device_state(&s);
+    if (st != LSE_OK) return st;
+    cudaError_t e = launch_conv2d_3x3(s->info, x, w, b, y, N, Cin, H, W, Cout, stream);
+    return e == cudaSuccess ? LSE_OK : cuda_fail(e);
+}
+
+lse_status_t conv_gn_act_lse(const float* x, const float* w, const float* b, const float* gamma,
+                             const float* beta, float* out, int64_t N, int64_t Cin, int64_t H, int64_t W,
+                             int64_t Cout, int64_t G, float eps, cudaStream_t stream) {
+    if (N < 0 || Cin <= 0 || Cout <= 0 || G <= 0 || H < 3 || W < 3 || Cout % G != 0) return LSE_ERR_SIZE;
+    int64_t nin = 0, ny = 0;
+    if (!mul_ok(N, Cin, &nin) || !mul_ok(nin, H, &nin) || !mul_ok(nin, W, &nin) || nin > INT64_MAX / 4 ||
+        !mul_ok(N, Cout, &ny) || !mul_ok(ny, (H - 2) * (W - 2), &ny) || ny > INT64_MAX / 4 || H > INT32_MAX ||
+        W > INT32_MAX)
+        return LSE_ERR_SIZE;
+    const int64_t cpg = Cout / G;
+    if (!conv_tc_supported(Cin, Cout) || Cin != 8 || 16 % cpg != 0 || G > 64) return LSE_ERR_UNSUPPORTED;
+    if (!(eps >= 0.f) || eps == __builtin_inff()) return LSE_ERR_VALUE;
+    if (ny == 0) return LSE_OK;
+    if (!x || !w || !b || !gamma || !beta || !out) return LSE_ERR_NULL;
+    if (!aligned4(x) || !aligned4(w) || !aligned4(b) || !aligned4(gamma) || !aligned4(beta) || !aligned4(out))
+        return LSE_ERR_ALIGN;
+    DeviceState* s = nullptr;
+    lse_status_t st = device_state(&s);
+    if (st != LSE_OK) return st;
+    cudaMemPool_t pool = nullptr;
+    if ((st = device_pool(s, &pool)) != LSE_OK) return st;
+    void* scratch = nullptr;
+    cudaError_t e =
+        cudaMallocFromPoolAsync(&scratch, conv_chain_scratch_bytes(N, H, W, Cout, G), pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_conv_gn_act_lse(s->info, x, w, b, gamma, beta, out, N, Cin, H, W, Cout, G, eps, scratch, stream);
+    cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (ef != cudaSuccess) return cuda_fail(ef);
+    return LSE_OK;
+}
+
 lse_status_t group_norm(const float* y, const float* gamma, const float* beta, float* out, int64_t N, int64_t C,
                         int64_t HW, int64_t G, float eps, cudaStream_t stream) {
     bool empty = false;

@@ -125,6 +125,42 @@ def test_gn_act_lse_validation(lib, args, want):
     assert lib.gn_act_residual(None, None, None, None, N, C, HW, G, eps, None) == want
 
 
+CONV_ERRORS = [
+    ((1, 8, 2, 8, 64), 2),        # H < 3
+    ((1, 0, 8, 8, 64), 2),        # Cin = 0
+    ((-1, 8, 8, 8, 64), 2),
+    ((1, 9, 8, 8, 64), 5),        # Cin > 8: no tensor-core path
+    ((1, 8, 8, 8, 40), 5),        # Cout not a multiple of 16
+    ((1, 8, 8, 8, 256), 5),       # Cout > 128
+    ((0, 8, 8, 8, 64), 0),        # no outputs
+    ((1, 8, 8, 8, 64), 1),        # null pointers
+]
+
+
+@pytest.mark.parametrize("args,want", CONV_ERRORS)
+def test_conv2d_validation(lib, args, want):
+    N, Cin, H, W, Cout = args
+    assert lib.conv2d_3x3(None, None, None, None, N, Cin, H, W, Cout, None) == want
+    assert lib.conv_gn_act_lse(None, None, None, None, None, None, N, Cin, H, W, Cout, 16 if Cout % 16 == 0
+                               else 1, 1e-5, None) == want
+
+
+CONV_CHAIN_ERRORS = [
+    ((1, 8, 8, 8, 64, 5, 1e-5), 2),     # Cout % G != 0
+    ((1, 8, 8, 8, 64, 2, 1e-5), 5),     # 32 channels per group: not a divisor of 16
+    ((1, 8, 8, 8, 64, 16, -1.0), 6),    # eps < 0
+    ((1, 8, 8, 8, 64, 0, 1e-5), 2),
+    ((1, 8, 8, 8, 64, 16, 1e-5), 1),    # null pointers
+    ((1, 4, 8, 8, 64, 16, 1e-5), 5),    # Cin != 8: conv2d_3x3 then gn_act_lse instead
+]
+
+
+@pytest.mark.parametrize("args,want", CONV_CHAIN_ERRORS)
+def test_conv_chain_validation(lib, args, want):
+    N, Cin, H, W, Cout, G, eps = args
+    assert lib.conv_gn_act_lse(None, None, None, None, None, None, N, Cin, H, W, Cout, G, eps, None) == want
+
+
 def test_binding_raises_on_error(lib):
     import torch
 

@@ -1,0 +1,154 @@
+"""Conv2d 3x3 on the tensor cores (and the chain fed by it) against the oracle,
+element by element, through the C ABI (GPU only)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from log_softmax_gb300 import build
+    build.build()
+    import log_softmax_gb300 as L
+    L.load_library()
+    torch.cuda.set_device(0)
+    yield L
+    assert L.lse_device_status() == 0
+
+
+def _inputs(N, Cin, H, W, Cout, seed=0):
+    inp = synth.make_inputs("conv_gn_act_lse_128x8x128x128", shape=(N, Cin, H, W))
+    if Cout != inp["w"].shape[0] or seed:
+        bound = 1.0 / np.sqrt(Cin * 9)
+        inp["w"] = synth.uniform((Cout, Cin, 3, 3), 300 + seed, -bound, bound)
+        inp["bias"] = synth.uniform((Cout,), 400 + seed, -bound, bound)
+        inp["gamma"] = synth.uniform((Cout,), 500 + seed, 0.5, 1.5)
+        inp["beta"] = synth.normal((Cout,), 600 + seed, var=0.1)
+    return inp
+
+
+def _conv(L, inp, misalign=False):
+    x, w, b = (inp[k].to(DEV) for k in ("x", "w", "bias"))
+    N, Cin, H, W = x.shape
+    Cout = w.shape[0]
+    y = torch.full((N, Cout, H - 2, W - 2), float("nan"), device=DEV)
+    if misalign:
+        def mis(t):
+            buf = torch.empty(t.numel() + 1, device=DEV)
+            v = buf[1:].view(t.shape)
+            v.copy_(t)
+            return v
+        x, w, b, y = mis(x), mis(w), mis(b), mis(y)
+    L.conv2d_3x3(x, w, b, y, N, Cin, H, W, Cout)
+    torch.cuda.synchronize()
+    return y.cpu()
+
+
+CONV_SHAPES = [
+    (2, 8, 16, 20, 64),     # several 128-pixel tiles, the chain's channel counts
+    (1, 8, 128, 128, 64),   # one full sample of the chain's input
+    (3, 3, 7, 9, 16),       # K = 27 padded to 32, one partial tile
+    (2, 1, 5, 5, 32),       # K = 9 padded to 16
+    (1, 8, 130, 131, 128),  # Cout = 128, ragged last tile
+    (5, 4, 12, 3, 48),      # OW = 1
+]
+
+
+@pytest.mark.parametrize("N,Cin,H,W,Cout", CONV_SHAPES)
+def test_conv2d_parity(lib, N, Cin, H, W, Cout):
+    inp = _inputs(N, Cin, H, W, Cout)
+    got = _conv(lib, inp)
+    ref = oracle.conv2d(inp["x"], inp["w"], inp["bias"])
+    assert_parity(got, ref, f"conv2d {N, Cin, H, W, Cout}")
+
+
+def test_conv2d_misaligned(lib):
+    inp = _inputs(2, 8, 9, 11, 64)
+    assert_parity(_conv(lib, inp, misalign=True), oracle.conv2d(inp["x"], inp["w"], inp["bias"]),
+                  "conv2d misaligned")
+
+
+def test_conv2d_wide_values(lib):
+    """Inputs of scale 30 and weights of scale 1: the split keeps fp32 accuracy.  Outputs
+    here are sums of products of scale ~15 whose fp32 accumulation alone rounds at ~1e-6
+    of the largest output, so the bar adds that term to the usual one."""
+    N, Cin, H, W, Cout = 2, 8, 10, 12, 64
+    inp = {"x": synth.normal((N, Cin, H, W), 71, var=900.0),
+           "w": synth.uniform((Cout, Cin, 3, 3), 72, -1.0, 1.0),
+           "bias": synth.normal((Cout,), 73)}
+    got = _conv(lib, inp)
+    ref = oracle.conv2d(inp["x"], inp["w"], inp["bias"])
+    err = np.abs(got.double().numpy() - ref)
+    assert (err <= 2e-5 + 2e-6 * np.abs(ref) + 1e-6 * np.abs(ref).max()).all(), err.max()
+
+
+def test_conv2d_forward_convenience(lib):
+    inp = _inputs(2, 8, 14, 15, 64)
+    got = lib.conv2d_3x3_forward(inp["x"].to(DEV), inp["w"].to(DEV), inp["bias"].to(DEV))
+    assert_parity(got, oracle.conv2d(inp["x"], inp["w"], inp["bias"]), "conv2d_3x3_forward")
+
+
+# ----------------------------------------------------------------------------- the chain from x
+
+CHAIN_CASES = [
+    (2, 8, 16, 20, 64, 16),     # the chain's channel counts, several tiles
+    (2, 8, 128, 128, 64, 16),   # two full samples of the chain's shape
+    (3, 8, 9, 11, 32, 8),       # 4 channels per group, Cout = 32
+    (2, 8, 12, 14, 64, 64),     # 1 channel per group
+    (2, 8, 12, 14, 64, 4),      # 16 channels per group
+    (1, 8, 20, 7, 48, 6),       # 8 channels per group, Cout = 48
+]
+
+
+def _chain(L, inp, G, eps=1e-5):
+    x, w, b, g, be = (inp[k].to(DEV) for k in ("x", "w", "bias", "gamma", "beta"))
+    N, Cin, H, W = x.shape
+    out = torch.full((N, 1, H - 2, W - 2), float("nan"), device=DEV)
+    L.conv_gn_act_lse(x, w, b, g, be, out, N, Cin, H, W, w.shape[0], G, eps)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+@pytest.mark.parametrize("N,Cin,H,W,Cout,G", CHAIN_CASES)
+def test_conv_chain_parity(lib, N, Cin, H, W, Cout, G):
+    inp = _inputs(N, Cin, H, W, Cout, seed=1 if Cout != 64 else 0)
+    got = _chain(lib, inp, G)
+    ref = oracle.conv_gn_act_lse(inp["x"], inp["w"], inp["bias"], inp["gamma"], inp["beta"], G, 1e-5)
+    assert_parity(got, ref, f"conv chain {N, Cin, H, W, Cout, G}")
+
+
+def test_conv_chain_other_cin_is_two_calls(lib):
+    """Cin other than the layer's 8 is not fused: the call reports it, and the two
+    calls it stands for give the chain."""
+    inp = _inputs(2, 3, 12, 10, 64, seed=2)
+    with pytest.raises(lib.LseError):
+        _chain(lib, inp, 16)
+    y = _conv(lib, inp).to(DEV)
+    got = lib.gn_act_lse_forward(y, inp["gamma"].to(DEV), inp["beta"].to(DEV), 16, 1e-5)
+    ref = oracle.conv_gn_act_lse(inp["x"], inp["w"], inp["bias"], inp["gamma"], inp["beta"], 16, 1e-5)
+    assert_parity(got, ref, "conv then chain, Cin = 3")
+
+
+def test_conv_chain_matches_two_steps(lib):
+    """The fused call equals conv2d_3x3 followed by gn_act_lse on its output."""
+    inp = _inputs(3, 8, 40, 36, 64)
+    y = _conv(lib, inp).to(DEV)
+    two = lib.gn_act_lse_forward(y, inp["gamma"].to(DEV), inp["beta"].to(DEV), 16, 1e-5).cpu()
+    one = _chain(lib, inp, 16)
+    assert (one - two).abs().max().item() < 1e-5
+
+
+def test_conv_chain_forward_convenience(lib):
+    inp = _inputs(2, 8, 18, 17, 64)
+    got = lib.conv_gn_act_lse_forward(*(inp[k].to(DEV) for k in ("x", "w", "bias", "gamma", "beta")), 16)
+    assert got.shape == (2, 1, 16, 15)
+    assert_parity(got, oracle.conv_gn_act_lse(inp["x"], inp["w"], inp["bias"], inp["gamma"], inp["beta"], 16),
+                  "conv_gn_act_lse_forward")
