@@ -167,12 +167,13 @@ lse_status_t gn_act_residual(const float* y, const float* gamma, const float* be
  *   x  [N * Cin * H * W] fp32 NCHW, device, read only.
  *   w  [Cout * Cin * 3 * 3] fp32, device, read only;  b [Cout] fp32, device.
  *   y  [N * Cout * (H-2) * (W-2)] fp32, device, written (must not alias x).
- *   N >= 0, H >= 3, W >= 3; 1 <= Cin <= 8 and Cout a multiple of 16 up to 128
- *   (else LSE_ERR_UNSUPPORTED).
- * Computed on the tensor cores as an implicit GEMM per 128-pixel tile with
- * every operand split into two tf32 parts (three products per pair), which
- * keeps fp32 accuracy: |err| <= 2e-5 + 1e-6 * |ref| against a double
- * evaluation for data of unit scale.
+ *   N >= 0, H >= 3, W >= 3; 1 <= Cin <= 8, Cout a multiple of 16 up to 128 and
+ *   W <= 1024 (else LSE_ERR_UNSUPPORTED).
+ * Computed on the tensor cores as nine shifted GEMMs (one per kernel tap) per
+ * tile of 128 output pixels, from one staged window of the input, with every
+ * operand split into two tf32 parts (three products per pair), which keeps
+ * fp32 accuracy: |err| <= 2e-5 + 1e-6 * |ref| against a double evaluation for
+ * data of unit scale.
  */
 lse_status_t conv2d_3x3(const float* x, const float* w, const float* b, float* y, int64_t N, int64_t Cin,
                         int64_t H, int64_t W, int64_t Cout, cudaStream_t stream);

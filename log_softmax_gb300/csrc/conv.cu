@@ -2,16 +2,19 @@
 // produces the y of the GroupNorm chain of the POPCORNBENCH page
 // "Kimi-K2.6 / l2_p92" (8 -> 64 channels on 128 x 128 planes).
 //
-// conv2d_tc_kernel: persistent CTAs of 128 threads loop over output tiles of
-// 128 pixels x Cout channels.  The weights are split (hi/lo tf32) into shared
-// memory once per CTA; per tile every thread writes the hi/lo patch row of one
-// pixel, one thread issues the 3xTF32 MMAs into tensor memory, and after their
-// commit every thread reads its pixel's Cout accumulators back (tcgen05.ld),
-// adds the bias and stores y with coalesced rows per channel.  With STATS the
-// epilogue also folds each channel group's values of the tile into a Welford
-// (count, mean, M2) -- per thread over the group's channels, then across the
-// tile's pixels by warp shuffles and shared memory -- and stores one partial
-// per (sample, tile, group); gn_tile_merge_kernel merges a sample's tiles.
+// conv2d_tc_kernel: persistent CTAs of NS tile slots (one warpgroup of 128
+// threads each, NS = 1..4 by shared memory); a slot loops over tiles of 128
+// wide pixels (conv_tile.cuh).  The weights are split (hi/lo tf32) into shared
+// memory once per CTA; per tile the slot's threads stage the input window (hi
+// and lo), one thread issues the 27 MMAs into the slot's tensor-memory
+// columns, and after their commit every thread reads its pixel's Cout
+// accumulators back (tcgen05.ld), adds the bias and stores y with coalesced
+// rows per channel.  The slots run independently, so one slot's loads overlap
+// another's MMAs and epilogue.  With CPG > 0 the epilogue also folds each
+// channel group's values of the tile into a Welford (count, mean, M2) -- per
+// thread over the group's channels, then across the tile's pixels through
+// shared memory -- and stores one partial per (sample, tile, group);
+// gn_tile_merge_kernel merges a sample's tiles.
 #include <algorithm>
 #include <cstdio>
 
@@ -29,53 +32,66 @@ struct ConvArgs {
     float* y;
     int64_t N;
     int cin, H, W, cout, OH, OW;
-    int64_t tiles;  // pixel tiles per sample
-    int G, cpg;     // channel groups of the statistics (STATS), cpg divides 16
-    float4* partials;  // [N][tiles][G] (count, mean, M2, 0) (STATS)
+    int64_t tiles;     // wide-pixel tiles per sample
+    int S;             // staged window (pixels)
+    int slots;         // tile slots per CTA
+    int tma;           // raw windows fetched by bulk copies one tile ahead (else direct loads)
+    int G, cpg;        // channel groups of the statistics (CPG > 0), cpg divides 16
+    float4* partials;  // [N][tiles][G] (count, mean, M2, 0) (CPG > 0)
     int* status;
 };
 
-// Tile slots per CTA: each slot is one warpgroup (128 threads) with its own
-// patch buffers and accumulator, working on its own tiles, so one slot's MMAs
-// and epilogue overlap the other's patch loads.
-constexpr int kConvSlots = 2;
+constexpr int kConvMaxSlots = 4;
 
-static size_t conv_smem_bytes(int cin, int cout) {
-    const int Kp = conv_kpad(cin);
-    return (size_t)kConvSlots * 2 * kConvTileM * Kp * 4 + (size_t)2 * cout * Kp * 4 + (size_t)(cout * 4 + 127) / 128 * 128;
+// Bytes of one slot: the window's hi and lo parts, or the statistics scratch
+// [G][128] float2 when that is larger (it reuses the same space).
+__host__ __device__ static inline size_t conv_slot_bytes(int S, int G) {
+    const size_t win = (size_t)S * 16 * 2 * 2, st = (size_t)G * kConvTileM * 8;
+    return win > st ? win : st;
+}
+
+// The raw window buffer of one slot (TMA path): 8 channel rows of S floats.
+__host__ __device__ static inline size_t conv_raw_bytes(int S) { return (size_t)S * 8 * 4; }
+
+__host__ __device__ static inline size_t conv_weight_bytes(int cout) {
+    return (size_t)cout * 9 * 8 * 4 * 2 + (size_t)(cout * 4 + 127) / 128 * 128;
 }
 
 __host__ __device__ static inline uint32_t conv_tmem_cols(int cout) { return cout <= 32 ? 32u : (cout <= 64 ? 64u : 128u); }
 
 template <int CIN, int CPG>
-__global__ void __launch_bounds__(kConvSlots * kConvTileM, 1) conv2d_tc_kernel(const ConvArgs a) {
+__global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kernel(const ConvArgs a) {
     constexpr bool STATS = CPG > 0;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ uint64_t bars[kConvSlots];
+    __shared__ uint64_t bars[kConvMaxSlots];
+    __shared__ uint64_t rawbars[kConvMaxSlots];
     __shared__ uint32_t tmem_slot;
-
-    constexpr int Kp = conv_kpad(CIN);
-    constexpr uint32_t kAbytes = kConvTileM * Kp * 4;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int slot = tid / kConvTileM, wtid = tid - slot * kConvTileM;  // warpgroup and thread in it
+    const int S = a.S, W = a.W;
     unsigned char* const bhi = smem_raw;
-    unsigned char* const blo = bhi + a.cout * Kp * 4;
-    float* const bias = reinterpret_cast<float*>(blo + a.cout * Kp * 4);
-    unsigned char* const ahi = smem_raw + (size_t)2 * a.cout * Kp * 4 + (size_t)((a.cout * 4 + 127) / 128 * 128) +
-                               (size_t)slot * 2 * kAbytes;
-    unsigned char* const alo = ahi + kAbytes;
-    // [group][pixel] (mean, M2) of the statistics epilogue, in this slot's patch
-    // buffers (free between the MMAs' completion and the next tile's patches)
-    float2* const wsm = reinterpret_cast<float2*>(ahi);
+    unsigned char* const blo = bhi + (size_t)a.cout * 9 * 8 * 4;
+    float* const bias = reinterpret_cast<float*>(blo + (size_t)a.cout * 9 * 8 * 4);
+    const size_t slot_bytes = conv_slot_bytes(S, STATS ? a.G : 0) + (a.tma ? conv_raw_bytes(S) : 0);
+    unsigned char* const ahi = smem_raw + conv_weight_bytes(a.cout) + (size_t)slot * slot_bytes;
+    unsigned char* const alo = ahi + (size_t)S * 16 * 2;
+    float* const raw = reinterpret_cast<float*>(ahi + conv_slot_bytes(S, STATS ? a.G : 0));
+    uint64_t* const rawbar = &rawbars[slot];
+    float2* const wsm = reinterpret_cast<float2*>(ahi);  // [group][pixel] (mean, M2), after the MMAs
     const uint32_t ncols = conv_tmem_cols(a.cout);
+    uint32_t alloc_cols = 32;
+    while (alloc_cols < ncols * (uint32_t)a.slots) alloc_cols <<= 1;
     uint64_t* const bar = &bars[slot];
 
-    if (warp == 0) tmem_alloc(&tmem_slot, ncols * kConvSlots);
+    if (warp == 0) tmem_alloc(&tmem_slot, alloc_cols);
     if (tid == 0) {
-        for (int k = 0; k < kConvSlots; ++k) mbar_init(&bars[k], 1);
+        for (int k = 0; k < a.slots; ++k) {
+            mbar_init(&bars[k], 1);
+            mbar_init(&rawbars[k], 1);
+        }
         fence_mbar_init();
     }
-    conv_stage_weights(a.w, a.cin, a.cout, bhi, blo, true);
+    conv_stage_weights(a.w, a.cin, a.cout, bhi, blo);
     for (int c = tid; c < a.cout; c += blockDim.x) bias[c] = a.b[c];
     fence_proxy_async_smem();  // the weights are read by the tensor cores (async proxy)
     tc_fence_before();
@@ -83,27 +99,48 @@ __global__ void __launch_bounds__(kConvSlots * kConvTileM, 1) conv2d_tc_kernel(c
     tc_fence_after();
     const uint32_t tmem = tmem_slot + (uint32_t)slot * ncols;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int64_t plane = (int64_t)a.H * W;
     const int64_t ohw = (int64_t)a.OH * a.OW;
     bool aborted = false;
     uint32_t phase = 0;
     const int bar_id = 1 + slot;  // named barrier of this warpgroup
 
-    for (int64_t t = (int64_t)blockIdx.x * kConvSlots + slot; t < a.N * a.tiles;
-         t += (int64_t)gridDim.x * kConvSlots) {
+    const int64_t first = (int64_t)blockIdx.x * a.slots + slot, step = (int64_t)gridDim.x * a.slots;
+    const int64_t total = a.N * a.tiles;
+    uint32_t raw_phase = 0;
+    if (a.tma && wtid == 0 && first < total) {
+        const int64_t n = first / a.tiles;
+        conv_fetch_window<CIN>(a.x + n * a.cin * plane, plane, (first - n * a.tiles) * kConvTileM, S, raw, rawbar);
+    }
+    for (int64_t t = first; t < total; t += step) {
         const int64_t n = t / a.tiles;
-        const int64_t p0 = (t - n * a.tiles) * kConvTileM;
-        conv_stage_patches<CIN>(a.x + n * CIN * a.H * a.W, a.H, a.W, a.OW, ohw, p0, wtid, ahi, alo, true);
+        const int64_t q0 = (t - n * a.tiles) * kConvTileM;  // first wide pixel of the tile
+        if (a.tma) {
+            mbar_wait_bounded(rawbar, raw_phase, aborted, a.status);
+            raw_phase ^= 1u;
+            conv_split_window<CIN>(raw, plane, q0, S, wtid, kConvTileM, ahi, alo);
+        } else {
+            conv_stage_window<CIN>(a.x + n * a.cin * plane, plane, q0, S, wtid, kConvTileM, ahi, alo);
+        }
         fence_proxy_async_smem();
-        named_bar_sync(bar_id, kConvTileM);  // the patches are in shared memory; D is free
+        named_bar_sync(bar_id, kConvTileM);  // the window is in shared memory, the raw buffer free; D is free
         if (wtid == 0) {
+            if (a.tma && t + step < total && !aborted) {  // the next tile's raw window, during this tile
+                const int64_t n2 = (t + step) / a.tiles;
+                conv_fetch_window<CIN>(a.x + n2 * a.cin * plane, plane, (t + step - n2 * a.tiles) * kConvTileM, S,
+                                       raw, rawbar);
+            }
             tc_fence_after();
-            conv_issue_mma(tmem, ahi, alo, bhi, blo, a.cin, a.cout, true, bar);
+            conv_issue_mma(tmem, ahi, alo, bhi, blo, W, S, a.cout, bar);
         }
         mbar_wait_bounded(bar, phase, aborted, a.status);
         phase ^= 1u;
         tc_fence_after();
-        const int64_t p = p0 + wtid;
-        const bool valid = p < ohw;
+        const int64_t q = q0 + wtid;
+        const int64_t oh = q / W;
+        const int ow = (int)(q - oh * W);
+        const bool valid = ow < a.OW && oh < a.OH;
+        const int64_t p = oh * a.OW + ow;
         float* dst = a.y + n * a.cout * ohw + p;
         for (int c0 = 0; c0 < a.cout; c0 += 16) {
             float v[16];
@@ -117,7 +154,7 @@ __global__ void __launch_bounds__(kConvSlots * kConvTileM, 1) conv2d_tc_kernel(c
             }
             if constexpr (STATS) {
                 // the 16 / CPG groups inside these 16 channels: exact mean and M2 of
-                // this pixel's CPG values of each
+                // this pixel's CPG values of each (the window is no longer read)
 #pragma unroll
                 for (int lo = 0; lo < 16; lo += CPG) {
                     float sum = 0.f;
@@ -127,7 +164,8 @@ __global__ void __launch_bounds__(kConvSlots * kConvTileM, 1) conv2d_tc_kernel(c
                     float m2 = 0.f;
 #pragma unroll
                     for (int j = 0; j < CPG; ++j) m2 = fmaf(v[lo + j] - mean, v[lo + j] - mean, m2);
-                    wsm[((c0 + lo) / CPG) * kConvTileM + wtid] = make_float2(mean, m2);
+                    wsm[((c0 + lo) / CPG) * kConvTileM + wtid] = valid ? make_float2(mean, m2)
+                                                                       : make_float2(0.f, -1.f);
                 }
             }
         }
@@ -142,8 +180,8 @@ __global__ void __launch_bounds__(kConvSlots * kConvTileM, 1) conv2d_tc_kernel(c
             Welford w{0.f, 0.f, 0.f};
             if (g < G) {
                 for (int m = j; m < kConvTileM; m += tpg) {
-                    const float2 q = wsm[g * kConvTileM + m];
-                    if (p0 + m < ohw) w = wf_merge(w, Welford{(float)CPG, q.x, q.y});
+                    const float2 qv = wsm[g * kConvTileM + m];
+                    if (qv.y >= 0.f) w = wf_merge(w, Welford{(float)CPG, qv.x, qv.y});  // M2 < 0 marks no pixel
                 }
             }
             for (int o = 1; o < tpg; o <<= 1) {
@@ -151,18 +189,24 @@ __global__ void __launch_bounds__(kConvSlots * kConvTileM, 1) conv2d_tc_kernel(c
                 w = wf_merge(w, other);
             }
             if (g < G && j == 0)
-                a.partials[(n * a.tiles + (p0 / kConvTileM)) * G + g] = make_float4(w.n, w.mean, w.m2, 0.f);
+                a.partials[(n * a.tiles + (q0 / kConvTileM)) * G + g] = make_float4(w.n, w.mean, w.m2, 0.f);
         }
         tc_fence_before();
-        named_bar_sync(bar_id, kConvTileM);  // this slot is done reading D, the patches and wsm
+        named_bar_sync(bar_id, kConvTileM);  // this slot is done reading D and its window / scratch
+    }
+    if (a.tma && wtid == 0 && aborted) {
+        // after a timeout the last raw fetch may still be in flight: one more bounded
+        // wait before the shared memory is released
+        bool again = false;
+        mbar_wait_bounded(rawbar, raw_phase, again, a.status);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem_slot, ncols * kConvSlots);
+    if (warp == 0) tmem_dealloc(tmem_slot, alloc_cols);
 }
 
-bool conv_tc_supported(int64_t cin, int64_t cout) {
-    return cin >= 1 && cin <= kConvMaxCin && cout >= 16 && cout <= 128 && cout % 16 == 0;
+bool conv_tc_supported(int64_t cin, int64_t cout, int64_t W) {
+    return cin >= 1 && cin <= kConvMaxCin && cout >= 16 && cout <= 128 && cout % 16 == 0 && W <= kConvMaxW;
 }
 
 template <int CIN, int CPG>
@@ -206,7 +250,10 @@ static ConvArgs conv_args(const DeviceInfo& dev, const float* x, const float* w,
     a.cout = (int)cout;
     a.OH = (int)H - 2;
     a.OW = (int)W - 2;
-    a.tiles = ((int64_t)a.OH * a.OW + kConvTileM - 1) / kConvTileM;
+    a.tiles = ((int64_t)a.OH * a.W + kConvTileM - 1) / kConvTileM;  // wide pixels
+    a.S = conv_window(a.W);
+    a.slots = 1;
+    a.tma = 0;
     a.G = 1;
     a.cpg = (int)cout;
     a.partials = nullptr;
@@ -220,33 +267,39 @@ cudaError_t launch_conv2d_3x3(const DeviceInfo& dev, const float* x, const float
 }
 
 template <int CIN, int CPG>
-static cudaError_t conv_go(const DeviceInfo& dev, const ConvArgs& a, cudaStream_t stream) {
+static cudaError_t conv_go(const DeviceInfo& dev, const ConvArgs& a0, cudaStream_t stream) {
     auto kern = conv2d_tc_kernel<CIN, CPG>;
-    const size_t smem = conv_smem_bytes(a.cin, a.cout);
+    ConvArgs a = a0;
+    // as many tile slots (up to 4) as shared and tensor memory hold
+    // raw windows by bulk copies when every plane starts 16-byte aligned
+    a.tma = ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0 && ((int64_t)a.H * a.W) % 4 == 0 &&
+             env_int("LSE_CONV_TMA", 1) != 0) ? 1 : 0;
+    const size_t wbytes = conv_weight_bytes(a.cout),
+                 sbytes = conv_slot_bytes(a.S, CPG > 0 ? a.G : 0) + (a.tma ? conv_raw_bytes(a.S) : 0);
+    const size_t budget = (size_t)dev.max_smem_optin - 1024;
+    if (wbytes + sbytes > budget) return cudaErrorNotSupported;
+    a.slots = (int)std::min<size_t>({(size_t)kConvMaxSlots, (budget - wbytes) / sbytes,
+                                     (size_t)(512 / conv_tmem_cols(a.cout))});
+    const size_t smem = wbytes + (size_t)a.slots * sbytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
+    const int threads = a.slots * kConvTileM;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kConvSlots * kConvTileM, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorNotSupported;
-    // tensor memory: per_sm CTAs x ncols columns must fit the SM's 512
-    per_sm = std::min<int>(per_sm, (int)(512 / (kConvSlots * conv_tmem_cols(a.cout))));
+    uint32_t alloc_cols = 32;
+    while (alloc_cols < conv_tmem_cols(a.cout) * (uint32_t)a.slots) alloc_cols <<= 1;
+    per_sm = std::min<int>(per_sm, (int)(512 / alloc_cols));  // tensor memory of co-resident CTAs
     const int64_t total = a.N * a.tiles;
-    const int64_t blocks = (total + kConvSlots - 1) / kConvSlots;
+    const int64_t blocks = (total + a.slots - 1) / a.slots;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)per_sm * dev.sm_count));
-    if (env_int("LSE_VERBOSE", 0)) {
-        cudaFuncAttributes fa;
-        cudaFuncGetAttributes(&fa, kern);
-        int smem_sm = 0, resv = 0;
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev.device);
-        cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev.device);
-        fprintf(stderr,
-                "[lse] conv2d_tc: grid=%u (%d per SM) tiles=%lld smem=%zu static=%zu regs=%d smem/SM=%d reserved=%d\n",
-                grid, per_sm, (long long)total, smem, fa.sharedSizeBytes, fa.numRegs, smem_sm, resv);
-    }
-    kern<<<grid, kConvSlots * kConvTileM, smem, stream>>>(a);
+    if (env_int("LSE_VERBOSE", 0))
+        fprintf(stderr, "[lse] conv2d_tc: grid=%u (%d per SM) slots=%d window=%d tma=%d tiles=%lld smem=%zu\n", grid,
+                per_sm, a.slots, a.S, a.tma, (long long)total, smem);
+    kern<<<grid, threads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -274,7 +327,7 @@ __global__ void __launch_bounds__(256) gn_tile_merge_kernel(const float4* __rest
 
 size_t conv_chain_scratch_bytes(int64_t N, int64_t H, int64_t W, int64_t cout, int64_t G) {
     const int64_t ohw = (H - 2) * (W - 2);
-    const int64_t tiles = (ohw + kConvTileM - 1) / kConvTileM;
+    const int64_t tiles = ((H - 2) * W + kConvTileM - 1) / kConvTileM;  // wide pixels
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
     return up((size_t)N * cout * ohw * 4) + up((size_t)N * tiles * G * sizeof(float4)) + up((size_t)N * G * 8);
 }

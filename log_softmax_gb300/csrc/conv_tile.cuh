@@ -1,26 +1,29 @@
-// One output tile of a 3x3, stride-1, valid convolution as an implicit GEMM on
-// the 5th-generation tensor cores (tcgen05, kind::tf32), for the Conv2d that
+// One output tile of a 3x3, stride-1, valid convolution as nine shifted GEMMs
+// on the 5th-generation tensor cores (tcgen05, kind::tf32), for the Conv2d that
 // feeds the GroupNorm chain of the POPCORNBENCH page "Kimi-K2.6 / l2_p92"
 // (8 -> 64 channels, kernel 3, no padding, bias).
 //
-// Tile: M = 128 consecutive output pixels of one sample (flattened oh * OW + ow)
-// by N = Cout output channels, K = Cin * 9 patch taps (padded with zeros to a
-// multiple of 8).  A (the im2col patches) and B (the weights) sit in shared
-// memory in the canonical K-major layout without swizzle: 8-row x 16-byte core
-// matrices, core matrices along M (or N) 128 bytes apart (stride byte offset)
-// and along K one full column of core matrices apart (leading byte offset).
-// The accumulator D (128 lanes x Cout fp32 columns) lives in tensor memory;
-// lane m holds pixel m, column c channel c, so an epilogue thread owns every
-// channel of one pixel.
+// Tiles run over "wide" pixels q = oh * W + ow with ow in [0, W) (the two
+// columns per row past OW are computed and dropped), so that output pixel q
+// reads input pixel q + u*W + v at tap (u, v).  A tile of M = 128 wide pixels
+// therefore needs only the input window [q0, q0 + 128 + 2W + 2) of each of the
+// Cin (padded to 8) channels, staged once in shared memory as two K-groups of 4
+// channels: element (channel c, window pixel s) at (c / 4) * LBO + s * 16 +
+// (c % 4) * 4.  That is the canonical K-major, no-swizzle operand layout (8
+// pixels x 16 bytes per core matrix, core matrices 128 bytes apart along M and
+// LBO apart along K), and the A operand of tap (u, v) is the same window with
+// its start address moved by (u*W + v) * 16 bytes: D += A_(u,v) B_(u,v) with
+// K = 8 per tap, nine taps per tile.  B_(u,v) = w[:, :, u, v] (Cout x 8) sits
+// in the same layout, one block per tap.  The accumulator D (128 lanes x Cout
+// fp32 columns) lives in tensor memory; lane m holds wide pixel q0 + m.
 //
 // Precision: a tf32 operand keeps 10 mantissa bits.  For results at fp32
 // accuracy every operand is split, a = hi + lo with hi = rn_tf32(a) and
 // lo = rn_tf32(a - hi), and D = A_hi B_hi + A_hi B_lo + A_lo B_hi ("3xTF32";
-// the dropped A_lo B_lo term is ~2^-22 relative).  A single A_hi B_hi pass,
-// with round-to-nearest operands (unbiased errors), serves where only sums
-// over many outputs are needed.
+// the dropped A_lo B_lo term is ~2^-22 relative).
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -28,17 +31,11 @@
 namespace lse {
 
 constexpr int kConvTileM = 128;
-constexpr int kConvMaxCin = 8;
-constexpr int kConvMaxK = 72;  // kConvMaxCin * 9, already a multiple of 8
+constexpr int kConvMaxCin = 8;  // channels padded to 8: one tf32 MMA (K = 8) per tap
+constexpr int kConvMaxW = 1024;
 
-// K padded to a multiple of 8 (one tf32 MMA consumes K = 8).
-__host__ __device__ constexpr int conv_kpad(int cin) { return (cin * 9 + 7) / 8 * 8; }
-
-// Byte offset of element (row r, tap k) in a K-major operand with `rows` rows
-// (a multiple of 8): core matrix (k / 4, r / 8), 8 rows of 16 bytes.
-__host__ __device__ constexpr uint32_t conv_kmajor_off(int r, int k, int rows) {
-    return (uint32_t)(((k >> 2) * (rows >> 3) + (r >> 3)) * 128 + (r & 7) * 16 + (k & 3) * 4);
-}
+// Staged window length (pixels, a multiple of 8) for input width W.
+__host__ __device__ constexpr int conv_window(int W) { return (kConvTileM + 2 * W + 2 + 7) / 8 * 8; }
 
 __device__ __forceinline__ uint32_t rn_tf32(float f) {
     uint32_t r;
@@ -107,74 +104,108 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// The weights w [Cout][Cin][3][3] as the B operand (N = Cout rows, K taps):
-// hi and lo parts (lo only when `split`), zero beyond K.  Whole CTA.
+// The weights w [Cout][Cin][3][3] as nine B operands, one per tap t = 3u + v:
+// element (co, c) of tap t at (2t + c / 4) * LBO_B + (co / 8) * 128 + (co % 8) * 16
+// + (c % 4) * 4 with LBO_B = Cout / 8 * 128; hi and lo parts, zero for c >= cin.
+// Whole CTA.
 __device__ __forceinline__ void conv_stage_weights(const float* __restrict__ w, int cin, int cout, unsigned char* bhi,
-                                                   unsigned char* blo, bool split) {
-    const int K = cin * 9, Kp = conv_kpad(cin);
-    for (int e = threadIdx.x; e < cout * Kp; e += blockDim.x) {
-        const int n = e / Kp, k = e - n * Kp;
-        const float v = k < K ? w[n * K + k] : 0.f;
+                                                   unsigned char* blo) {
+    const uint32_t lbo = (uint32_t)(cout / 8) * 128;
+    for (int e = threadIdx.x; e < cout * 9 * 8; e += blockDim.x) {
+        const int co = e / 72, t = (e / 8) % 9, c = e % 8;
+        const float v = c < cin ? w[(co * cin + c) * 9 + t] : 0.f;
         const uint32_t hi = rn_tf32(v);
-        const uint32_t off = conv_kmajor_off(n, k, cout);
+        const uint32_t off = (uint32_t)(2 * t + c / 4) * lbo + (uint32_t)(co / 8) * 128 + (co % 8) * 16 + (c % 4) * 4;
         *reinterpret_cast<uint32_t*>(bhi + off) = hi;
-        if (split) *reinterpret_cast<uint32_t*>(blo + off) = rn_tf32(v - __uint_as_float(hi));
+        *reinterpret_cast<uint32_t*>(blo + off) = rn_tf32(v - __uint_as_float(hi));
     }
 }
 
-// Thread m (0..127) writes row m of the A operand (the patch of output pixel
-// p = p0 + m of sample plane xs = x + n*CIN*H*W), hi and lo parts (lo only
-// when `split`); pixels past the plane's end get zero rows.  All of the row's
-// loads are issued before the first is used (one latency per tile).
+// The input window [q0, q0 + S) of one sample (planes xs[c * plane + q]) as
+// the A operand, hi and lo parts; pixels past the plane and channels >= CIN are
+// zero.  Threads t, t + nt, ... of the calling group each take one window pixel:
+// CIN coalesced loads, then two 16-byte stores per part.
 template <int CIN>
-__device__ __forceinline__ void conv_stage_patches(const float* __restrict__ xs, int H, int W, int OW, int64_t ohw,
-                                                   int64_t p0, int m, unsigned char* ahi, unsigned char* alo,
-                                                   bool split) {
-    constexpr int K = CIN * 9, KP = conv_kpad(CIN);
-    const int64_t p = p0 + m;
-    const bool valid = p < ohw;
-    const int oh = valid ? (int)(p / OW) : 0, ow = valid ? (int)(p - (int64_t)oh * OW) : 0;
-    const float* base = xs + (int64_t)oh * W + ow;
-    const int64_t plane = (int64_t)H * W;
-    float v[KP];
+__device__ __forceinline__ void conv_stage_window(const float* __restrict__ xs, int64_t plane, int64_t q0, int S,
+                                                  int t, int nt, unsigned char* ahi, unsigned char* alo) {
+    const uint32_t lbo = (uint32_t)S * 16;
+    for (int s = t; s < S; s += nt) {
+        const int64_t q = q0 + s;
+        const bool in = q < plane;
+        float v[8];
 #pragma unroll
-    for (int k = 0; k < KP; ++k) {
-        const int ci = k / 9, t = k - (k / 9) * 9, u = t / 3, vv = t - (t / 3) * 3;
-        v[k] = (valid && k < K) ? __ldg(base + ci * plane + u * W + vv) : 0.f;
-    }
+        for (int c = 0; c < 8; ++c) v[c] = (c < CIN && in) ? __ldg(xs + c * plane + q) : 0.f;
 #pragma unroll
-    for (int k0 = 0; k0 < KP; k0 += 4) {
-        uint4 hi;
-        hi.x = rn_tf32(v[k0]); hi.y = rn_tf32(v[k0 + 1]); hi.z = rn_tf32(v[k0 + 2]); hi.w = rn_tf32(v[k0 + 3]);
-        const uint32_t off = conv_kmajor_off(m, k0, kConvTileM);
-        *reinterpret_cast<uint4*>(ahi + off) = hi;
-        if (split) {
-            uint4 lo;
-            lo.x = rn_tf32(v[k0] - __uint_as_float(hi.x));
-            lo.y = rn_tf32(v[k0 + 1] - __uint_as_float(hi.y));
-            lo.z = rn_tf32(v[k0 + 2] - __uint_as_float(hi.z));
-            lo.w = rn_tf32(v[k0 + 3] - __uint_as_float(hi.w));
+        for (int kg = 0; kg < 2; ++kg) {
+            uint4 hi, lo;
+            hi.x = rn_tf32(v[4 * kg + 0]); hi.y = rn_tf32(v[4 * kg + 1]);
+            hi.z = rn_tf32(v[4 * kg + 2]); hi.w = rn_tf32(v[4 * kg + 3]);
+            lo.x = rn_tf32(v[4 * kg + 0] - __uint_as_float(hi.x));
+            lo.y = rn_tf32(v[4 * kg + 1] - __uint_as_float(hi.y));
+            lo.z = rn_tf32(v[4 * kg + 2] - __uint_as_float(hi.z));
+            lo.w = rn_tf32(v[4 * kg + 3] - __uint_as_float(hi.w));
+            const uint32_t off = kg * lbo + (uint32_t)s * 16;
+            *reinterpret_cast<uint4*>(ahi + off) = hi;
             *reinterpret_cast<uint4*>(alo + off) = lo;
         }
     }
 }
 
-// One thread: the MMAs of a tile into D at d_tmem.  split: A_hi B_hi + A_hi B_lo
-// + A_lo B_hi per K-step of 8; else A_hi B_hi.  Then a commit on `bar`.
-__device__ __forceinline__ void conv_issue_mma(uint32_t d_tmem, const unsigned char* ahi, const unsigned char* alo,
-                                               const unsigned char* bhi, const unsigned char* blo, int cin, int cout,
-                                               bool split, uint64_t* bar) {
-    const int Kp = conv_kpad(cin);
-    const uint32_t idesc = umma_idesc_tf32(kConvTileM, cout);
-    const uint32_t lbo_a = (kConvTileM / 8) * 128, lbo_b = (uint32_t)(cout / 8) * 128;
-    const uint32_t sa_hi = smem_u32(ahi), sa_lo = smem_u32(alo), sb_hi = smem_u32(bhi), sb_lo = smem_u32(blo);
-    for (int i = 0; i < Kp / 8; ++i) {
-        const uint32_t oa = 2u * i * lbo_a, ob = 2u * i * lbo_b;
-        umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, i > 0);
-        if (split) {
-            umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_lo + ob, lbo_b, 128), idesc, 1);
-            umma_tf32(d_tmem, umma_desc(sa_lo + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, 1);
+// One thread: bulk copies (TMA) of the raw input window [q0, q0 + S) of CIN
+// channel planes into raw[c][S] (the part inside the plane; the rest is never
+// read), completing on `bar`.  Needs 16-byte aligned planes (x aligned,
+// plane % 4 == 0) and q0 % 4 == 0.
+template <int CIN>
+__device__ __forceinline__ void conv_fetch_window(const float* __restrict__ xs, int64_t plane, int64_t q0, int S,
+                                                  float* raw, uint64_t* bar) {
+    const int64_t n = std::min<int64_t>(S, plane - q0);
+    const uint32_t bytes = (uint32_t)n * 4u;
+    mbar_arrive_expect_tx(bar, bytes * CIN);
+#pragma unroll
+    for (int c = 0; c < CIN; ++c) bulk_g2s(raw + (size_t)c * S, xs + c * plane + q0, bytes, bar);
+}
+
+// The raw window (raw[c][S], valid up to plane - q0) as the A operand, hi and
+// lo parts, zero past the plane and for channels >= CIN.  Threads t, t + nt, ...
+template <int CIN>
+__device__ __forceinline__ void conv_split_window(const float* raw, int64_t plane, int64_t q0, int S, int t, int nt,
+                                                  unsigned char* ahi, unsigned char* alo) {
+    const uint32_t lbo = (uint32_t)S * 16;
+    for (int s = t; s < S; s += nt) {
+        const bool in = q0 + s < plane;
+        float v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = (c < CIN && in) ? raw[c * S + s] : 0.f;
+#pragma unroll
+        for (int kg = 0; kg < 2; ++kg) {
+            uint4 hi, lo;
+            hi.x = rn_tf32(v[4 * kg + 0]); hi.y = rn_tf32(v[4 * kg + 1]);
+            hi.z = rn_tf32(v[4 * kg + 2]); hi.w = rn_tf32(v[4 * kg + 3]);
+            lo.x = rn_tf32(v[4 * kg + 0] - __uint_as_float(hi.x));
+            lo.y = rn_tf32(v[4 * kg + 1] - __uint_as_float(hi.y));
+            lo.z = rn_tf32(v[4 * kg + 2] - __uint_as_float(hi.z));
+            lo.w = rn_tf32(v[4 * kg + 3] - __uint_as_float(hi.w));
+            const uint32_t off = kg * lbo + (uint32_t)s * 16;
+            *reinterpret_cast<uint4*>(ahi + off) = hi;
+            *reinterpret_cast<uint4*>(alo + off) = lo;
         }
+    }
+}
+
+// One thread: the 27 MMAs of a tile (nine taps, three products each) into D at
+// d_tmem, then a commit on `bar`.
+__device__ __forceinline__ void conv_issue_mma(uint32_t d_tmem, const unsigned char* ahi, const unsigned char* alo,
+                                               const unsigned char* bhi, const unsigned char* blo, int W, int S,
+                                               int cout, uint64_t* bar) {
+    const uint32_t idesc = umma_idesc_tf32(kConvTileM, cout);
+    const uint32_t lbo_a = (uint32_t)S * 16, lbo_b = (uint32_t)(cout / 8) * 128;
+    const uint32_t sa_hi = smem_u32(ahi), sa_lo = smem_u32(alo), sb_hi = smem_u32(bhi), sb_lo = smem_u32(blo);
+#pragma unroll
+    for (int t = 0; t < 9; ++t) {
+        const uint32_t oa = (uint32_t)((t / 3) * W + (t % 3)) * 16, ob = 2u * t * lbo_b;
+        umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, t > 0);
+        umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_lo + ob, lbo_b, 128), idesc, 1);
+        umma_tf32(d_tmem, umma_desc(sa_lo + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, 1);
     }
     umma_commit(bar);
 }

@@ -102,8 +102,8 @@ cudaError_t launch_gn_tma(const DeviceInfo& dev, const float* y, const float* ga
 
 // Conv2d 3 x 3, stride 1, valid, with bias, on the tensor cores (3xTF32):
 // x [N, cin, H, W] -> y [N, cout, H - 2, W - 2].  Shapes conv_tc_supported()
-// accepts: 1 <= cin <= 8, cout a multiple of 16 up to 128.
-bool conv_tc_supported(int64_t cin, int64_t cout);
+// accepts: 1 <= cin <= 8, cout a multiple of 16 up to 128, W <= 1024.
+bool conv_tc_supported(int64_t cin, int64_t cout, int64_t W);
 cudaError_t launch_conv2d_3x3(const DeviceInfo& dev, const float* x, const float* w, const float* b, float* y,
                               int64_t N, int64_t cin, int64_t H, int64_t W, int64_t cout, cudaStream_t stream);
 

@@ -313,7 +313,7 @@ lse_status_t conv2d_3x3(const float* x, const float* w, const float* b, float* y
         !mul_ok(N, Cout, &nout) || !mul_ok(nout, (H - 2) * (W - 2), &nout) || nout > INT64_MAX / 4 ||
         H > INT32_MAX || W > INT32_MAX)
         return LSE_ERR_SIZE;
-    if (!conv_tc_supported(Cin, Cout)) return LSE_ERR_UNSUPPORTED;
+    if (!conv_tc_supported(Cin, Cout, W)) return LSE_ERR_UNSUPPORTED;
     if (nout == 0) return LSE_OK;
     if (!x || !w || !b || !y) return LSE_ERR_NULL;
     if (!aligned4(x) || !aligned4(w) || !aligned4(b) || !aligned4(y)) return LSE_ERR_ALIGN;
@@ -334,7 +334,7 @@ lse_status_t conv_gn_act_lse(const float* x, const float* w, const float* b, con
         W > INT32_MAX)
         return LSE_ERR_SIZE;
     const int64_t cpg = Cout / G;
-    if (!conv_tc_supported(Cin, Cout) || Cin != 8 || 16 % cpg != 0 || G > 64) return LSE_ERR_UNSUPPORTED;
+    if (!conv_tc_supported(Cin, Cout, W) || Cin != 8 || 16 % cpg != 0 || G > 64) return LSE_ERR_UNSUPPORTED;
     if (!(eps >= 0.f) || eps == __builtin_inff()) return LSE_ERR_VALUE;
     if (ny == 0) return LSE_OK;
     if (!x || !w || !b || !gamma || !beta || !out) return LSE_ERR_NULL;

@@ -132,6 +132,7 @@ CONV_ERRORS = [
     ((1, 9, 8, 8, 64), 5),        # Cin > 8: no tensor-core path
     ((1, 8, 8, 8, 40), 5),        # Cout not a multiple of 16
     ((1, 8, 8, 8, 256), 5),       # Cout > 128
+    ((1, 8, 8, 1025, 64), 5),     # W > 1024: the staged window would not fit
     ((0, 8, 8, 8, 64), 0),        # no outputs
     ((1, 8, 8, 8, 64), 1),        # null pointers
 ]

@@ -152,3 +152,12 @@ def test_conv_chain_forward_convenience(lib):
     assert got.shape == (2, 1, 16, 15)
     assert_parity(got, oracle.conv_gn_act_lse(inp["x"], inp["w"], inp["bias"], inp["gamma"], inp["beta"], 16),
                   "conv_gn_act_lse_forward")
+
+
+@pytest.mark.parametrize("tma", ["0", "1"])
+def test_conv2d_window_paths(lib, tma, monkeypatch):
+    """Raw windows fetched by bulk copies one tile ahead, or loaded directly."""
+    monkeypatch.setenv("LSE_CONV_TMA", tma)
+    for shape in ((3, 8, 20, 24, 64), (1, 8, 130, 132, 64), (2, 3, 9, 12, 16)):
+        inp = _inputs(*shape, seed=3)
+        assert_parity(_conv(lib, inp), oracle.conv2d(inp["x"], inp["w"], inp["bias"]), f"conv tma={tma} {shape}")
