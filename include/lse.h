@@ -188,9 +188,13 @@ lse_status_t conv2d_3x3(const float* x, const float* w, const float* b, float* y
  *   finite; the
  *   conv2d_3x3 shape rules.  Other shapes: conv2d_3x3 then gn_act_lse.
  * The convolution's epilogue writes y and the Welford partials of every
- * (sample, 128-pixel tile, group), so the statistics never re-read y; the
- * apply pass reads y once.  Scratch (y itself, about N*Cout*(H-2)*(W-2)*4
- * bytes, plus the partials) comes from the library's pool on `stream`.
+ * (sample, 128-pixel tile, group), so the statistics never re-read y; after
+ * they are merged the apply pass reads y once.  Scratch (y itself, about
+ * N*Cout*(H-2)*(W-2)*4 bytes, plus the partials) comes from the library's pool
+ * on `stream`.  (LSE_CONV_CHAIN=2 selects a form where y never reaches memory:
+ * the convolution runs twice and the second pass finishes the chain from the
+ * tensor-core accumulators; it is slower on GB300 while the convolution is
+ * bound by its tensor work.)
  */
 lse_status_t conv_gn_act_lse(const float* x, const float* w, const float* b, const float* gamma,
                              const float* beta, float* out, int64_t N, int64_t Cin, int64_t H, int64_t W,

@@ -14,7 +14,10 @@
 // channel group's values of the tile into a Welford (count, mean, M2) -- per
 // thread over the group's channels, then across the tile's pixels through
 // shared memory -- and stores one partial per (sample, tile, group);
-// gn_tile_merge_kernel merges a sample's tiles.
+// gn_tile_merge_kernel merges a sample's tiles.  The statistics mode uses one
+// product of round-to-nearest tf32 operands (unbiased errors of ~2^-12
+// relative per product average out over the ~63,000 values of a group: mean
+// and variance stay within ~1e-5 relative), the other modes the 3xTF32 split.
 #include <algorithm>
 #include <cstdio>
 
@@ -37,9 +40,20 @@ struct ConvArgs {
     int slots;         // tile slots per CTA
     int tma;           // raw windows fetched by bulk copies one tile ahead (else direct loads)
     int G, cpg;        // channel groups of the statistics (CPG > 0), cpg divides 16
-    float4* partials;  // [N][tiles][G] (count, mean, M2, 0) (CPG > 0)
+    float4* partials;  // [N][tiles][G] (count, mean, M2, 0) (statistics mode)
+    const float* stats;  // [N][G] (mean, 1/sqrt(var + eps)) (apply mode)
+    const float* gamma;  // [cout] (apply mode)
+    const float* beta;   // [cout] (apply mode)
+    float* out;          // [N][OH * OW] channel lse (apply mode)
     int* status;
 };
+
+// What the epilogue does with the tile's accumulators.
+//   kConvWriteY       y (3xTF32)
+//   kConvStats        per-(tile, group) Welford partials only (one tf32 product)
+//   kConvApplyLse     the chain finished from the accumulators (3xTF32)
+//   kConvWriteYStats  y and the partials (3xTF32)
+enum ConvMode { kConvWriteY = 0, kConvStats = 1, kConvApplyLse = 2, kConvWriteYStats = 3 };
 
 constexpr int kConvMaxSlots = 4;
 
@@ -53,15 +67,20 @@ __host__ __device__ static inline size_t conv_slot_bytes(int S, int G) {
 // The raw window buffer of one slot (TMA path): 8 channel rows of S floats.
 __host__ __device__ static inline size_t conv_raw_bytes(int S) { return (size_t)S * 8 * 4; }
 
+// The apply mode's per-channel table of one slot.
+__host__ __device__ static inline size_t conv_tab_bytes(int cout) { return (size_t)cout * 16; }
+
 __host__ __device__ static inline size_t conv_weight_bytes(int cout) {
     return (size_t)cout * 9 * 8 * 4 * 2 + (size_t)(cout * 4 + 127) / 128 * 128;
 }
 
 __host__ __device__ static inline uint32_t conv_tmem_cols(int cout) { return cout <= 32 ? 32u : (cout <= 64 ? 64u : 128u); }
 
-template <int CIN, int CPG>
+template <int CIN, int CPG, int MODE>
 __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kernel(const ConvArgs a) {
-    constexpr bool STATS = CPG > 0;
+    constexpr bool STATS = MODE == kConvStats || MODE == kConvWriteYStats;
+    constexpr bool ONE_PRODUCT = MODE == kConvStats;
+    constexpr bool APPLY = MODE == kConvApplyLse;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t bars[kConvMaxSlots];
     __shared__ uint64_t rawbars[kConvMaxSlots];
@@ -72,10 +91,13 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
     unsigned char* const bhi = smem_raw;
     unsigned char* const blo = bhi + (size_t)a.cout * 9 * 8 * 4;
     float* const bias = reinterpret_cast<float*>(blo + (size_t)a.cout * 9 * 8 * 4);
-    const size_t slot_bytes = conv_slot_bytes(S, STATS ? a.G : 0) + (a.tma ? conv_raw_bytes(S) : 0);
+    const size_t win_bytes = conv_slot_bytes(S, STATS ? a.G : 0);
+    const size_t slot_bytes = win_bytes + (a.tma ? conv_raw_bytes(S) : 0) + (APPLY ? conv_tab_bytes(a.cout) : 0);
     unsigned char* const ahi = smem_raw + conv_weight_bytes(a.cout) + (size_t)slot * slot_bytes;
     unsigned char* const alo = ahi + (size_t)S * 16 * 2;
-    float* const raw = reinterpret_cast<float*>(ahi + conv_slot_bytes(S, STATS ? a.G : 0));
+    float* const raw = reinterpret_cast<float*>(ahi + win_bytes);
+    // apply mode: the sample's per-channel table {mean, rstd*gamma*2log2e, beta*2log2e, 0}
+    float4* const tab = reinterpret_cast<float4*>(ahi + win_bytes + (a.tma ? conv_raw_bytes(S) : 0));
     uint64_t* const rawbar = &rawbars[slot];
     float2* const wsm = reinterpret_cast<float2*>(ahi);  // [group][pixel] (mean, M2), after the MMAs
     const uint32_t ncols = conv_tmem_cols(a.cout);
@@ -118,7 +140,7 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
         if (a.tma) {
             mbar_wait_bounded(rawbar, raw_phase, aborted, a.status);
             raw_phase ^= 1u;
-            conv_split_window<CIN>(raw, plane, q0, S, wtid, kConvTileM, ahi, alo);
+            conv_split_window<CIN, !ONE_PRODUCT>(raw, plane, q0, S, wtid, kConvTileM, ahi, alo);
         } else {
             conv_stage_window<CIN>(a.x + n * a.cin * plane, plane, q0, S, wtid, kConvTileM, ahi, alo);
         }
@@ -131,7 +153,18 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
                                        raw, rawbar);
             }
             tc_fence_after();
-            conv_issue_mma(tmem, ahi, alo, bhi, blo, W, S, a.cout, bar);
+            conv_issue_mma(tmem, ahi, alo, bhi, blo, W, S, a.cout, !ONE_PRODUCT, bar);
+        }
+        if constexpr (APPLY) {
+            // the table of sample n, while the MMAs run (the previous tile's readers
+            // passed the slot barrier at its end)
+            const int cpg = a.cpg;
+            for (int c = wtid; c < a.cout; c += kConvTileM) {
+                const int64_t g = n * a.G + c / cpg;
+                const float mean = a.stats[2 * g], rstd = a.stats[2 * g + 1];
+                tab[c] = make_float4(mean, rstd * a.gamma[c] * (2.f * kLog2e), a.beta[c] * (2.f * kLog2e), 0.f);
+            }
+            named_bar_sync(bar_id, kConvTileM);
         }
         mbar_wait_bounded(bar, phase, aborted, a.status);
         phase ^= 1u;
@@ -141,16 +174,25 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
         const int ow = (int)(q - oh * W);
         const bool valid = ow < a.OW && oh < a.OH;
         const int64_t p = oh * a.OW + ow;
-        float* dst = a.y + n * a.cout * ohw + p;
+        MS st = ms_empty();
         for (int c0 = 0; c0 < a.cout; c0 += 16) {
             float v[16];
             tmem_ld16(tmem + lane_base + (uint32_t)c0, v);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += bias[c0 + j];
-            if (valid) {
+            if constexpr (MODE == kConvWriteY || MODE == kConvWriteYStats) {
+                if (valid) {
+                    float* dst = a.y + n * a.cout * ohw + p;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) dst[(int64_t)(c0 + j) * ohw] = v[j];
+                    for (int j = 0; j < 16; ++j) dst[(int64_t)(c0 + j) * ohw] = v[j];
+                }
+            }
+            if constexpr (APPLY) {
+                // z, tanh, hardswish, + y, then the online channel lse
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = act_residual(v[j], tab[c0 + j]);
+                ms_fold<16>(st, v);
             }
             if constexpr (STATS) {
                 // the 16 / CPG groups inside these 16 channels: exact mean and M2 of
@@ -168,6 +210,9 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
                                                                        : make_float2(0.f, -1.f);
                 }
             }
+        }
+        if constexpr (APPLY) {
+            if (valid) a.out[n * ohw + p] = ms_lse(st);
         }
         if constexpr (STATS) {
             // merge over the tile's pixels: tpg threads per group, each a strided
@@ -209,30 +254,31 @@ bool conv_tc_supported(int64_t cin, int64_t cout, int64_t W) {
     return cin >= 1 && cin <= kConvMaxCin && cout >= 16 && cout <= 128 && cout % 16 == 0 && W <= kConvMaxW;
 }
 
-template <int CIN, int CPG>
+template <int CIN, int CPG, int MODE>
 static cudaError_t conv_go(const DeviceInfo& dev, const ConvArgs& a, cudaStream_t stream);
 
 static cudaError_t conv_dispatch(const DeviceInfo& dev, const ConvArgs& a, cudaStream_t stream) {
     switch (a.cin) {
-        case 1: return conv_go<1, 0>(dev, a, stream);
-        case 2: return conv_go<2, 0>(dev, a, stream);
-        case 3: return conv_go<3, 0>(dev, a, stream);
-        case 4: return conv_go<4, 0>(dev, a, stream);
-        case 5: return conv_go<5, 0>(dev, a, stream);
-        case 6: return conv_go<6, 0>(dev, a, stream);
-        case 7: return conv_go<7, 0>(dev, a, stream);
-        default: return conv_go<8, 0>(dev, a, stream);
+        case 1: return conv_go<1, 0, kConvWriteY>(dev, a, stream);
+        case 2: return conv_go<2, 0, kConvWriteY>(dev, a, stream);
+        case 3: return conv_go<3, 0, kConvWriteY>(dev, a, stream);
+        case 4: return conv_go<4, 0, kConvWriteY>(dev, a, stream);
+        case 5: return conv_go<5, 0, kConvWriteY>(dev, a, stream);
+        case 6: return conv_go<6, 0, kConvWriteY>(dev, a, stream);
+        case 7: return conv_go<7, 0, kConvWriteY>(dev, a, stream);
+        default: return conv_go<8, 0, kConvWriteY>(dev, a, stream);
     }
 }
 
-// The statistics epilogue is compiled for the chain's own convolution (Cin = 8).
+// The chain's epilogues are compiled for its own convolution (Cin = 8).
+template <int MODE>
 static cudaError_t conv_stats_dispatch(const DeviceInfo& dev, const ConvArgs& a, cudaStream_t stream) {
     switch (a.cpg) {
-        case 1: return conv_go<8, 1>(dev, a, stream);
-        case 2: return conv_go<8, 2>(dev, a, stream);
-        case 4: return conv_go<8, 4>(dev, a, stream);
-        case 8: return conv_go<8, 8>(dev, a, stream);
-        default: return conv_go<8, 16>(dev, a, stream);
+        case 1: return conv_go<8, 1, MODE>(dev, a, stream);
+        case 2: return conv_go<8, 2, MODE>(dev, a, stream);
+        case 4: return conv_go<8, 4, MODE>(dev, a, stream);
+        case 8: return conv_go<8, 8, MODE>(dev, a, stream);
+        default: return conv_go<8, 16, MODE>(dev, a, stream);
     }
 }
 
@@ -257,6 +303,10 @@ static ConvArgs conv_args(const DeviceInfo& dev, const float* x, const float* w,
     a.G = 1;
     a.cpg = (int)cout;
     a.partials = nullptr;
+    a.stats = nullptr;
+    a.gamma = nullptr;
+    a.beta = nullptr;
+    a.out = nullptr;
     a.status = dev.status;
     return a;
 }
@@ -266,16 +316,18 @@ cudaError_t launch_conv2d_3x3(const DeviceInfo& dev, const float* x, const float
     return conv_dispatch(dev, conv_args(dev, x, w, b, y, N, cin, H, W, cout), stream);
 }
 
-template <int CIN, int CPG>
+template <int CIN, int CPG, int MODE>
 static cudaError_t conv_go(const DeviceInfo& dev, const ConvArgs& a0, cudaStream_t stream) {
-    auto kern = conv2d_tc_kernel<CIN, CPG>;
+    auto kern = conv2d_tc_kernel<CIN, CPG, MODE>;
     ConvArgs a = a0;
     // as many tile slots (up to 4) as shared and tensor memory hold
     // raw windows by bulk copies when every plane starts 16-byte aligned
     a.tma = ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0 && ((int64_t)a.H * a.W) % 4 == 0 &&
              env_int("LSE_CONV_TMA", 1) != 0) ? 1 : 0;
     const size_t wbytes = conv_weight_bytes(a.cout),
-                 sbytes = conv_slot_bytes(a.S, CPG > 0 ? a.G : 0) + (a.tma ? conv_raw_bytes(a.S) : 0);
+                 sbytes = conv_slot_bytes(a.S, (MODE == kConvStats || MODE == kConvWriteYStats) ? a.G : 0) +
+                          (a.tma ? conv_raw_bytes(a.S) : 0) +
+                          (MODE == kConvApplyLse ? conv_tab_bytes(a.cout) : 0);
     const size_t budget = (size_t)dev.max_smem_optin - 1024;
     if (wbytes + sbytes > budget) return cudaErrorNotSupported;
     a.slots = (int)std::min<size_t>({(size_t)kConvMaxSlots, (budget - wbytes) / sbytes,
@@ -325,34 +377,51 @@ __global__ void __launch_bounds__(256) gn_tile_merge_kernel(const float4* __rest
     }
 }
 
+// Two ways through the chain: by default the convolution writes y with the
+// partials and the GroupNorm apply pass reads y once (HBM: x, y twice, out);
+// with LSE_CONV_CHAIN=2 y never reaches memory -- a one-product pass for the
+// partials, then the convolution again, finishing the chain from tensor memory
+// (HBM: x twice, out; twice the tensor work).
+static bool conv_chain_y_free() { return env_int("LSE_CONV_CHAIN", 1) == 2; }
+
 size_t conv_chain_scratch_bytes(int64_t N, int64_t H, int64_t W, int64_t cout, int64_t G) {
-    const int64_t ohw = (H - 2) * (W - 2);
     const int64_t tiles = ((H - 2) * W + kConvTileM - 1) / kConvTileM;  // wide pixels
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-    return up((size_t)N * cout * ohw * 4) + up((size_t)N * tiles * G * sizeof(float4)) + up((size_t)N * G * 8);
+    const size_t y = conv_chain_y_free() ? 0 : up((size_t)N * cout * (H - 2) * (W - 2) * 4);
+    return y + up((size_t)N * tiles * G * sizeof(float4)) + up((size_t)N * G * 8);
 }
 
 cudaError_t launch_conv_gn_act_lse(const DeviceInfo& dev, const float* x, const float* w, const float* b,
                                    const float* gamma, const float* beta, float* out, int64_t N, int64_t cin,
                                    int64_t H, int64_t W, int64_t cout, int64_t G, float eps, void* scratch,
                                    cudaStream_t stream) {
-    const int64_t ohw = (H - 2) * (W - 2);
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    const bool y_free = conv_chain_y_free();
+    const int64_t ohw = (H - 2) * (W - 2);
     char* sp = static_cast<char*>(scratch);
-    float* y = reinterpret_cast<float*>(sp);
-    sp += up((size_t)N * cout * ohw * 4);
+    float* y = y_free ? nullptr : reinterpret_cast<float*>(sp);
+    if (!y_free) sp += up((size_t)N * cout * ohw * 4);
     ConvArgs a = conv_args(dev, x, w, b, y, N, cin, H, W, cout);
     a.G = (int)G;
     a.cpg = (int)(cout / G);
     a.partials = reinterpret_cast<float4*>(sp);
-    sp += up((size_t)N * a.tiles * G * sizeof(float4));
-    float* stats = reinterpret_cast<float*>(sp);
-    cudaError_t e = conv_stats_dispatch(dev, a, stream);
+    float* stats = reinterpret_cast<float*>(sp + up((size_t)N * a.tiles * G * sizeof(float4)));
+    // 1: the convolution with each tile's per-group Welford partials (and y)
+    cudaError_t e = y_free ? conv_stats_dispatch<kConvStats>(dev, a, stream)
+                           : conv_stats_dispatch<kConvWriteYStats>(dev, a, stream);
     if (e != cudaSuccess) return e;
+    // 2: per-(n, g) mean and 1/sqrt(var + eps)
     const int64_t NG = N * G;
     gn_tile_merge_kernel<<<(unsigned)((NG + 7) / 8), 256, 0, stream>>>(a.partials, stats, NG, a.tiles, (int)G, eps);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return launch_gn_apply(dev, y, gamma, beta, out, N, cout, ohw, G, stats, stream);
+    // 3: the GroupNorm apply pass over y, or the convolution again finishing the
+    //    chain from tensor memory
+    if (!y_free) return launch_gn_apply(dev, y, gamma, beta, out, N, cout, ohw, G, stats, stream);
+    a.stats = stats;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.out = out;
+    return conv_go<8, 0, kConvApplyLse>(dev, a, stream);
 }
 
 }  // namespace lse

@@ -167,7 +167,7 @@ __device__ __forceinline__ void conv_fetch_window(const float* __restrict__ xs, 
 
 // The raw window (raw[c][S], valid up to plane - q0) as the A operand, hi and
 // lo parts, zero past the plane and for channels >= CIN.  Threads t, t + nt, ...
-template <int CIN>
+template <int CIN, bool SPLIT = true>
 __device__ __forceinline__ void conv_split_window(const float* raw, int64_t plane, int64_t q0, int S, int t, int nt,
                                                   unsigned char* ahi, unsigned char* alo) {
     const uint32_t lbo = (uint32_t)S * 16;
@@ -178,25 +178,30 @@ __device__ __forceinline__ void conv_split_window(const float* raw, int64_t plan
         for (int c = 0; c < 8; ++c) v[c] = (c < CIN && in) ? raw[c * S + s] : 0.f;
 #pragma unroll
         for (int kg = 0; kg < 2; ++kg) {
-            uint4 hi, lo;
+            uint4 hi;
             hi.x = rn_tf32(v[4 * kg + 0]); hi.y = rn_tf32(v[4 * kg + 1]);
             hi.z = rn_tf32(v[4 * kg + 2]); hi.w = rn_tf32(v[4 * kg + 3]);
-            lo.x = rn_tf32(v[4 * kg + 0] - __uint_as_float(hi.x));
-            lo.y = rn_tf32(v[4 * kg + 1] - __uint_as_float(hi.y));
-            lo.z = rn_tf32(v[4 * kg + 2] - __uint_as_float(hi.z));
-            lo.w = rn_tf32(v[4 * kg + 3] - __uint_as_float(hi.w));
             const uint32_t off = kg * lbo + (uint32_t)s * 16;
             *reinterpret_cast<uint4*>(ahi + off) = hi;
-            *reinterpret_cast<uint4*>(alo + off) = lo;
+            if constexpr (SPLIT) {
+                uint4 lo;
+                lo.x = rn_tf32(v[4 * kg + 0] - __uint_as_float(hi.x));
+                lo.y = rn_tf32(v[4 * kg + 1] - __uint_as_float(hi.y));
+                lo.z = rn_tf32(v[4 * kg + 2] - __uint_as_float(hi.z));
+                lo.w = rn_tf32(v[4 * kg + 3] - __uint_as_float(hi.w));
+                *reinterpret_cast<uint4*>(alo + off) = lo;
+            }
         }
     }
 }
 
-// One thread: the 27 MMAs of a tile (nine taps, three products each) into D at
-// d_tmem, then a commit on `bar`.
+// One thread: the MMAs of a tile (nine taps; with `split` three products each,
+// else the hi parts alone) into D at d_tmem, then a commit on `bar`.  The
+// tensor pipe's time per MMA does not shrink with N, so at N = 64 the products
+// are the conv's bound: the single-product form costs a third.
 __device__ __forceinline__ void conv_issue_mma(uint32_t d_tmem, const unsigned char* ahi, const unsigned char* alo,
                                                const unsigned char* bhi, const unsigned char* blo, int W, int S,
-                                               int cout, uint64_t* bar) {
+                                               int cout, bool split, uint64_t* bar) {
     const uint32_t idesc = umma_idesc_tf32(kConvTileM, cout);
     const uint32_t lbo_a = (uint32_t)S * 16, lbo_b = (uint32_t)(cout / 8) * 128;
     const uint32_t sa_hi = smem_u32(ahi), sa_lo = smem_u32(alo), sb_hi = smem_u32(bhi), sb_lo = smem_u32(blo);
@@ -204,8 +209,10 @@ __device__ __forceinline__ void conv_issue_mma(uint32_t d_tmem, const unsigned c
     for (int t = 0; t < 9; ++t) {
         const uint32_t oa = (uint32_t)((t / 3) * W + (t % 3)) * 16, ob = 2u * t * lbo_b;
         umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, t > 0);
-        umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_lo + ob, lbo_b, 128), idesc, 1);
-        umma_tf32(d_tmem, umma_desc(sa_lo + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, 1);
+        if (split) {
+            umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_lo + ob, lbo_b, 128), idesc, 1);
+            umma_tf32(d_tmem, umma_desc(sa_lo + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, 1);
+        }
     }
     umma_commit(bar);
 }

@@ -117,8 +117,10 @@ def _chain(L, inp, G, eps=1e-5):
     return out.cpu()
 
 
+@pytest.mark.parametrize("chain", ["1", "2"], ids=["y-round-trip", "y-free"])
 @pytest.mark.parametrize("N,Cin,H,W,Cout,G", CHAIN_CASES)
-def test_conv_chain_parity(lib, N, Cin, H, W, Cout, G):
+def test_conv_chain_parity(lib, N, Cin, H, W, Cout, G, chain, monkeypatch):
+    monkeypatch.setenv("LSE_CONV_CHAIN", chain)
     inp = _inputs(N, Cin, H, W, Cout, seed=1 if Cout != 64 else 0)
     got = _chain(lib, inp, G)
     ref = oracle.conv_gn_act_lse(inp["x"], inp["w"], inp["bias"], inp["gamma"], inp["beta"], G, 1e-5)
