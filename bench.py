@@ -502,7 +502,8 @@ def run_ours(args, w: synth.Workload):
     launch_ms = statistics.mean(per_step_ms)
     achieved = nbytes / (launch_ms / 1e3) / 1e9
     dominant = LAUNCHES[w.op][0]
-    achieved_note = "one launch per step"
+    achieved_note = ("one launch per step" if len(LAUNCHES[w.op]) == 1 else
+                     f"{len(LAUNCHES[w.op])} launches per step ({', '.join(LAUNCHES[w.op])}); achieved over the whole step")
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dominant, w.name),
                 "kernel": dominant, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
