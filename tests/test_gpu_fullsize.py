@@ -1,4 +1,4 @@
-"""The five workloads at full size, in the launch configuration the bench times
+"""The bench workloads at full size, in the launch configuration the bench times
 (GPU only).  Outputs the oracle can afford are checked element by element on a
 seeded sample; every output is checked against properties that hold at any size.
 """
@@ -97,3 +97,85 @@ def test_gn_act_lse_128x64x126x126(lib):
     ymax = y.amax(dim=1, keepdim=True)
     assert bool((out <= ymax + 2.0 / 3.0 + math.log(C) + 1e-4).all())
     assert bool((out >= ymax - 1.0 / 3.0 - 1e-4).all())
+
+
+# ----------------------------------------------------------------------------- the NEXT rows at full size
+
+def test_softmax_4096x393216(lib):
+    rows, cols = 4096, 393216
+    x = synth.make_inputs("softmax_4096x393216", device=DEV)["x"]
+    out = torch.empty_like(x)
+    lib.softmax_lastdim(x, out, rows, cols)
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(505)
+    rows_s = sorted(set([0, rows - 1] + torch.randint(0, rows, (6,), generator=g).tolist()))
+    assert_parity(out[rows_s].cpu(), oracle.softmax(x[rows_s].cpu()), "sampled rows")
+    # every row sums to one, every entry in [0, 1]
+    for r0 in range(0, rows, 512):
+        s = out[r0:r0 + 512].double().sum(dim=1)
+        assert bool(((s - 1).abs() < 1e-4).all()), float((s - 1).abs().max())
+    assert bool(((out >= 0) & (out <= 1)).all())
+    del x, out
+
+
+def test_log_softmax_dim0_32x8192x4096(lib):
+    x = synth.make_inputs("log_softmax_dim0_32x8192x4096", device=DEV)["x"]
+    R, inner = 32, 8192 * 4096
+    out = torch.empty_like(x)
+    lib.log_softmax_dim(x, out, 1, R, inner)
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(606)
+    idx = torch.cat([torch.randint(0, inner, (4096,), generator=g),
+                     torch.tensor([0, 1, 2, 3, inner - 4, inner - 3, inner - 2, inner - 1])]).to(DEV)
+    cols = x.view(R, inner)[:, idx].cpu().contiguous()
+    assert_parity(out.view(R, inner)[:, idx].cpu(), oracle.log_softmax_dim(cols, 1, R, cols.shape[1])[0],
+                  "sampled columns")
+    # every column: sum over the axis of exp = 1
+    for c0 in range(0, inner, 1 << 24):
+        s = torch.exp(out.view(R, inner)[:, c0:c0 + (1 << 24)].double()).sum(dim=0)
+        assert bool(((s - 1).abs() < 1e-5).all()), float((s - 1).abs().max())
+    del x, out
+
+
+@pytest.mark.parametrize("fn,workload", [("group_norm", "group_norm_128x64x126x126"),
+                                         ("gn_act_residual", "gn_act_residual_128x64x126x126")])
+def test_gn_elementwise_full(lib, fn, workload):
+    inp = synth.make_inputs(workload, device=DEV)
+    y, gamma, beta = inp["y"], inp["gamma"], inp["beta"]
+    N, C, H, W = y.shape
+    out = torch.empty_like(y)
+    getattr(lib, fn)(y, gamma, beta, out, N, C, H * W, 16, 1e-5)
+    torch.cuda.synchronize()
+    for n in (0, 64, N - 1):
+        ref = getattr(oracle, fn)(y[n:n + 1].cpu(), gamma.cpu(), beta.cpu(), 16, 1e-5)
+        assert_parity(out[n:n + 1].cpu(), ref, f"{fn} sample {n}")
+    if fn == "group_norm":
+        # every (n, g): ((z - beta) / gamma) has mean 0 and variance var / (var + eps)
+        zn = ((out - beta.view(1, C, 1, 1)) / gamma.view(1, C, 1, 1)).double().view(N, 16, -1)
+        var = y.double().view(N, 16, -1).var(dim=2, unbiased=False)
+        assert float(zn.mean(dim=2).abs().max()) < 1e-4
+        assert float((zn.var(dim=2, unbiased=False) - var / (var + 1e-5)).abs().max()) < 1e-4
+    else:
+        # every element: out - y = hardswish(tanh(z)) lies in [-1/3, 2/3]
+        d = out - y
+        assert bool(((d >= -1.0 / 3.0 - 1e-6) & (d <= 2.0 / 3.0 + 1e-6)).all())
+    del y, out
+
+
+def test_conv_gn_act_lse_128x8x128x128(lib):
+    inp = synth.make_inputs("conv_gn_act_lse_128x8x128x128", device=DEV)
+    x, w, b, gamma, beta = (inp[k] for k in ("x", "w", "bias", "gamma", "beta"))
+    N, Cin, H, W = x.shape
+    out = torch.empty(N, 1, H - 2, W - 2, device=DEV)
+    lib.conv_gn_act_lse(x, w, b, gamma, beta, out, N, Cin, H, W, 64, 16, 1e-5)
+    torch.cuda.synchronize()
+    for n in (0, 91, N - 1):
+        ref = oracle.conv_gn_act_lse(x[n:n + 1].cpu(), w.cpu(), b.cpu(), gamma.cpu(), beta.cpu(), 16, 1e-5)
+        assert_parity(out[n:n + 1].cpu(), ref, f"conv chain sample {n}")
+    # every output: the chain's bounds around max_c y (y from the library's conv)
+    y = torch.empty(N, 64, H - 2, W - 2, device=DEV)
+    lib.conv2d_3x3(x, w, b, y, N, Cin, H, W, 64)
+    ymax = y.amax(dim=1, keepdim=True)
+    assert bool((out <= ymax + 2.0 / 3.0 + math.log(64) + 1e-4).all())
+    assert bool((out >= ymax - 1.0 / 3.0 - 1e-4).all())
+    del x, y, out
