@@ -257,6 +257,7 @@ struct GnFusedArgs {
     float4* partials;          // [N][G][parts] (count, mean, M2, -)
     unsigned* done;            // [N] statistics parts finished, zero at launch
     unsigned long long* next;  // work-item counter, zero at launch
+    unsigned stats_target;     // statistics parts an apply tile waits for (G * parts)
     int* status;
 };
 
@@ -324,12 +325,12 @@ __global__ void __launch_bounds__(T) gn_fused_kernel(const GnFusedArgs a) {
                 red_release_gpu_add(a.done + n, 1u);
             }
         } else {
-            if (tid == 0 && !aborted && ld_acquire_gpu_u32(a.done + n) < (unsigned)GP) {
+            if (tid == 0 && !aborted && ld_acquire_gpu_u32(a.done + n) < a.stats_target) {
                 const uint64_t t0 = globaltimer_ns();
                 bool ok = false;
                 for (uint32_t it = 0; it < (1u << 26); ++it) {
                     __nanosleep(64);
-                    if (ld_acquire_gpu_u32(a.done + n) >= (unsigned)GP) {
+                    if (ld_acquire_gpu_u32(a.done + n) >= a.stats_target) {
                         ok = true;
                         break;
                     }
@@ -471,6 +472,10 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     args.C = (int)C;
     args.G = (int)G;
     args.parts = gn_parts();
+    // LSE_TEST_UNREACHABLE_WAIT=1 asks for one statistics part more than exist, so
+    // every apply tile's bounded wait runs out (~1 s) and the kernel records
+    // LSE_ERR_TIMEOUT: the failure path, exercised without a fault or a hang.
+    args.stats_target = (unsigned)(G * args.parts) + (env_int("LSE_TEST_UNREACHABLE_WAIT", 0) == 1 ? 1u : 0u);
     const int T = out_kind == 0 ? env_int("LSE_GN_THREADS", 256) : 256;
     args.tiles = (int)((HW + (int64_t)T * VEC - 1) / ((int64_t)T * VEC));
     args.lag = (int)std::min<int64_t>(N, std::max(0, env_int("LSE_GN_LAG", 16)));

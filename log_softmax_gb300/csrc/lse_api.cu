@@ -114,6 +114,17 @@ lse_status_t host_pipe(DeviceState* s, HostPipe** out) {
     return LSE_OK;
 }
 
+// Stream-ordered scratch from the device pool.  LSE_TEST_FAIL_ALLOC=1 makes it
+// fail as an exhausted pool would (cudaErrorMemoryAllocation), so that the
+// error path of every entry point can be exercised without using up memory.
+cudaError_t pool_alloc(void** p, size_t bytes, cudaMemPool_t pool, cudaStream_t stream) {
+    if (env_int("LSE_TEST_FAIL_ALLOC", 0) == 1) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
+
 bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -188,7 +199,7 @@ lse_status_t row_transform(const float* x, float* out, int64_t rows, int64_t col
                 cudaMemPool_t pool = nullptr;
                 if ((st = device_pool(s, &pool)) != LSE_OK) return st;
                 void* scratch = nullptr;
-                e = cudaMallocFromPoolAsync(&scratch, plan.scratch_bytes, pool, stream);
+                e = pool_alloc(&scratch, plan.scratch_bytes, pool, stream);
                 if (e != cudaSuccess) return cuda_fail(e);
                 e = kind == 5 ? launch_lsm_l2_group(s->info, x, out, rows, cols, plan, scratch, stream)
                   : kind == 6 ? launch_lsm_ws_group(s->info, x, out, rows, cols, plan, scratch, stream, softmax)
@@ -257,7 +268,7 @@ lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, flo
     const bool want_tma = variant == 3 || (variant != 2 && out_kind != 0);
     const bool tma = want_tma && gn_tma_applies(s->info, y, out, C, HW);
     void* scratch = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&scratch, tma ? gn_tma_scratch_bytes(N, G) : gn_fused_scratch_bytes(N, G),
+    cudaError_t e = pool_alloc(&scratch, tma ? gn_tma_scratch_bytes(N, G) : gn_fused_scratch_bytes(N, G),
                                             pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     if (tma)
@@ -347,7 +358,7 @@ lse_status_t conv_gn_act_lse(const float* x, const float* w, const float* b, con
     if ((st = device_pool(s, &pool)) != LSE_OK) return st;
     void* scratch = nullptr;
     cudaError_t e =
-        cudaMallocFromPoolAsync(&scratch, conv_chain_scratch_bytes(N, H, W, Cout, G), pool, stream);
+        pool_alloc(&scratch, conv_chain_scratch_bytes(N, H, W, Cout, G), pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     e = launch_conv_gn_act_lse(s->info, x, w, b, gamma, beta, out, N, Cin, H, W, Cout, G, eps, scratch, stream);
     cudaError_t ef = cudaFreeAsync(scratch, stream);
@@ -386,7 +397,7 @@ lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, f
     cudaMemPool_t pool = nullptr;
     if ((st = device_pool(s, &pool)) != LSE_OK) return st;
     void* stats = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&stats, (size_t)N * G * 2 * sizeof(float), pool, stream);
+    cudaError_t e = pool_alloc(&stats, (size_t)N * G * 2 * sizeof(float), pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     e = launch_gn_act_lse(s->info, y, gamma, beta, out, N, C, HW, G, eps, static_cast<float*>(stats), stream);
     cudaError_t ef = cudaFreeAsync(stats, stream);
@@ -422,7 +433,7 @@ lse_status_t log_softmax_lastdim_host(const float* x, float* out, int64_t rows, 
 
     std::lock_guard<std::mutex> lock(hp->mu);
     void* mem = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&mem, 2 * kHostBufs * buf_bytes, pool, stream);
+    cudaError_t e = pool_alloc(&mem, 2 * kHostBufs * buf_bytes, pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     auto din = [&](int b) { return reinterpret_cast<float*>(static_cast<char*>(mem) + (size_t)b * buf_bytes); };
     auto dout = [&](int b) {
