@@ -217,10 +217,11 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_sha(kernel: str) -> str:
-    """sha256 (first 16 hex digits) over the kernel's source files, common.cuh and launch.h."""
+    """sha256 (first 16 hex digits) over the kernel's source files and common.cuh (the
+    device code it is built from; launch.h holds host declarations only)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "log_softmax_gb300", "csrc")
-    for f in sorted(KERNEL_SOURCES[kernel] + ["common.cuh", "launch.h"]):
+    for f in sorted(KERNEL_SOURCES[kernel] + ["common.cuh"]):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
