@@ -320,6 +320,24 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
+def host_cpu() -> str:
+    """The host's logical core count and CPU model (for the CPU baseline's record)."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        import platform
+        model = platform.machine()
+    return f"{os.cpu_count()} logical cores, {model}"
+
+
 def time_oracle(w: synth.Workload, sample, budget_s: float, unit: int):
     """Runs the oracle over successive slices of `unit` rows / columns / samples of
     the host sample, cycling through it, until budget_s has passed.  Returns
@@ -415,7 +433,8 @@ def run_reference(args, w: synth.Workload):
         "config": {"workload": w.name, "shape": list(w.shape), "recipe": w.recipe,
                    "sample_per_step": sample},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample + " per step (single-threaded C, double precision)"},
+                         "sample": sample + " per step (single-threaded C, double precision)",
+                         "host": host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -524,7 +543,7 @@ def run_ours(args, w: synth.Workload):
         b, s, units = time_oracle(w, sample, budget_s=args.cpu_seconds, unit=unit)
         what = sample_text(w, sample, units)
         cpu = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": what + f", {s:.1f} s single-threaded"}
+               "sample": what + f", {s:.1f} s single-threaded", "host": host_cpu()}
 
     if rank != 0:
         return 0
