@@ -74,7 +74,14 @@ __host__ __device__ static inline size_t conv_weight_bytes(int cout) {
     return (size_t)cout * 9 * 8 * 4 * 2 + (size_t)(cout * 4 + 127) / 128 * 128;
 }
 
-__host__ __device__ static inline uint32_t conv_tmem_cols(int cout) { return cout <= 32 ? 32u : (cout <= 64 ? 64u : 128u); }
+// Accumulator columns of one slot (2 Cout when the products are stacked), a
+// power of two >= 32.
+__host__ __device__ static inline uint32_t conv_tmem_cols(int cout) {
+    const uint32_t need = (uint32_t)(conv_stacked(cout) ? 2 * cout : cout);
+    uint32_t n = 32;
+    while (n < need) n <<= 1;
+    return n;
+}
 
 template <int CIN, int CPG, int MODE>
 __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kernel(const ConvArgs a) {
@@ -88,9 +95,8 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
     const int tid = threadIdx.x, warp = tid >> 5;
     const int slot = tid / kConvTileM, wtid = tid - slot * kConvTileM;  // warpgroup and thread in it
     const int S = a.S, W = a.W;
-    unsigned char* const bhi = smem_raw;
-    unsigned char* const blo = bhi + (size_t)a.cout * 9 * 8 * 4;
-    float* const bias = reinterpret_cast<float*>(blo + (size_t)a.cout * 9 * 8 * 4);
+    unsigned char* const bw = smem_raw;  // the nine B operands, hi and lo rows
+    float* const bias = reinterpret_cast<float*>(bw + (size_t)a.cout * 9 * 8 * 4 * 2);
     const size_t win_bytes = conv_slot_bytes(S, STATS ? a.G : 0);
     const size_t slot_bytes = win_bytes + (a.tma ? conv_raw_bytes(S) : 0) + (APPLY ? conv_tab_bytes(a.cout) : 0);
     unsigned char* const ahi = smem_raw + conv_weight_bytes(a.cout) + (size_t)slot * slot_bytes;
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
         }
         fence_mbar_init();
     }
-    conv_stage_weights(a.w, a.cin, a.cout, bhi, blo);
+    conv_stage_weights(a.w, a.cin, a.cout, bw);
     for (int c = tid; c < a.cout; c += blockDim.x) bias[c] = a.b[c];
     fence_proxy_async_smem();  // the weights are read by the tensor cores (async proxy)
     tc_fence_before();
@@ -153,7 +159,7 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
                                        raw, rawbar);
             }
             tc_fence_after();
-            conv_issue_mma(tmem, ahi, alo, bhi, blo, W, S, a.cout, !ONE_PRODUCT, bar);
+            conv_issue_mma(tmem, ahi, alo, bw, W, S, a.cout, !ONE_PRODUCT, bar);
         }
         if constexpr (APPLY) {
             // the table of sample n, while the MMAs run (the previous tile's readers
@@ -178,7 +184,15 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
         for (int c0 = 0; c0 < a.cout; c0 += 16) {
             float v[16];
             tmem_ld16(tmem + lane_base + (uint32_t)c0, v);
-            tmem_wait_ld();
+            if (!ONE_PRODUCT && conv_stacked(a.cout)) {
+                float vl[16];  // the A_hi B_lo half
+                tmem_ld16(tmem + lane_base + (uint32_t)(a.cout + c0), vl);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += vl[j];
+            } else {
+                tmem_wait_ld();
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += bias[c0 + j];
             if constexpr (MODE == kConvWriteY || MODE == kConvWriteYStats) {

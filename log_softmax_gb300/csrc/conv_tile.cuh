@@ -20,7 +20,12 @@
 // Precision: a tf32 operand keeps 10 mantissa bits.  For results at fp32
 // accuracy every operand is split, a = hi + lo with hi = rn_tf32(a) and
 // lo = rn_tf32(a - hi), and D = A_hi B_hi + A_hi B_lo + A_lo B_hi ("3xTF32";
-// the dropped A_lo B_lo term is ~2^-22 relative).
+// the dropped A_lo B_lo term is ~2^-22 relative).  B_hi and B_lo of a tap are
+// stacked along N; for Cout <= 64 the first two products are one MMA of
+// N = 2 Cout into columns [0, 2 Cout) and A_lo B_hi a second of N = Cout into
+// [0, Cout), the epilogue adding the two halves (A_hi is read once per tap).
+// Wider layers keep three MMAs of N = Cout into one accumulator, whose Cout
+// columns leave room for more tile slots in tensor memory.
 #pragma once
 
 #include <algorithm>
@@ -104,20 +109,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// The weights w [Cout][Cin][3][3] as nine B operands, one per tap t = 3u + v:
-// element (co, c) of tap t at (2t + c / 4) * LBO_B + (co / 8) * 128 + (co % 8) * 16
-// + (c % 4) * 4 with LBO_B = Cout / 8 * 128; hi and lo parts, zero for c >= cin.
-// Whole CTA.
-__device__ __forceinline__ void conv_stage_weights(const float* __restrict__ w, int cin, int cout, unsigned char* bhi,
-                                                   unsigned char* blo) {
-    const uint32_t lbo = (uint32_t)(cout / 8) * 128;
+// The weights w [Cout][Cin][3][3] as nine B operands, one per tap t = 3u + v,
+// each 2 Cout rows (row co the hi part of output channel co, row Cout + co its
+// lo part) by 8 channels: element (row r, channel c) of tap t at
+// (2t + c / 4) * LBO_B + (r / 8) * 128 + (r % 8) * 16 + (c % 4) * 4 with
+// LBO_B = 2 Cout / 8 * 128; zero for c >= cin.  Whole CTA.
+__host__ __device__ constexpr uint32_t conv_lbo_b(int cout) { return (uint32_t)(2 * cout / 8) * 128; }
+
+// Whether a tile's first two products run as one MMA of N = 2 Cout.
+__host__ __device__ constexpr bool conv_stacked(int cout) { return cout <= 64; }
+
+__device__ __forceinline__ void conv_stage_weights(const float* __restrict__ w, int cin, int cout,
+                                                   unsigned char* b) {
+    const uint32_t lbo = conv_lbo_b(cout);
     for (int e = threadIdx.x; e < cout * 9 * 8; e += blockDim.x) {
         const int co = e / 72, t = (e / 8) % 9, c = e % 8;
         const float v = c < cin ? w[(co * cin + c) * 9 + t] : 0.f;
         const uint32_t hi = rn_tf32(v);
-        const uint32_t off = (uint32_t)(2 * t + c / 4) * lbo + (uint32_t)(co / 8) * 128 + (co % 8) * 16 + (c % 4) * 4;
-        *reinterpret_cast<uint32_t*>(bhi + off) = hi;
-        *reinterpret_cast<uint32_t*>(blo + off) = rn_tf32(v - __uint_as_float(hi));
+        const uint32_t plane = (uint32_t)(2 * t + c / 4) * lbo + (c % 4) * 4;
+        const int rlo = cout + co;
+        *reinterpret_cast<uint32_t*>(b + plane + (uint32_t)(co / 8) * 128 + (co % 8) * 16) = hi;
+        *reinterpret_cast<uint32_t*>(b + plane + (uint32_t)(rlo / 8) * 128 + (rlo % 8) * 16) =
+            rn_tf32(v - __uint_as_float(hi));
     }
 }
 
@@ -195,23 +208,25 @@ __device__ __forceinline__ void conv_split_window(const float* raw, int64_t plan
     }
 }
 
-// One thread: the MMAs of a tile (nine taps; with `split` three products each,
-// else the hi parts alone) into D at d_tmem, then a commit on `bar`.  The
-// tensor pipe's time per MMA does not shrink with N, so at N = 64 the products
-// are the conv's bound: the single-product form costs a third.
+// One thread: the MMAs of a tile into D at d_tmem, then a commit on `bar`.
+// Without `split`, the hi parts alone (N = Cout).  With it, stacked: A_hi
+// [B_hi; B_lo] (N = 2 Cout, columns [0, 2 Cout)) and A_lo B_hi (N = Cout,
+// columns [0, Cout)); else A_hi B_hi, A_hi B_lo and A_lo B_hi, all N = Cout.
 __device__ __forceinline__ void conv_issue_mma(uint32_t d_tmem, const unsigned char* ahi, const unsigned char* alo,
-                                               const unsigned char* bhi, const unsigned char* blo, int W, int S,
-                                               int cout, bool split, uint64_t* bar) {
-    const uint32_t idesc = umma_idesc_tf32(kConvTileM, cout);
-    const uint32_t lbo_a = (uint32_t)S * 16, lbo_b = (uint32_t)(cout / 8) * 128;
-    const uint32_t sa_hi = smem_u32(ahi), sa_lo = smem_u32(alo), sb_hi = smem_u32(bhi), sb_lo = smem_u32(blo);
+                                               const unsigned char* b, int W, int S, int cout, bool split,
+                                               uint64_t* bar) {
+    const bool stacked = split && conv_stacked(cout);
+    const uint32_t idesc = umma_idesc_tf32(kConvTileM, cout), idesc2 = umma_idesc_tf32(kConvTileM, 2 * cout);
+    const uint32_t lbo_a = (uint32_t)S * 16, lbo_b = conv_lbo_b(cout), lo_rows = (uint32_t)(cout / 8) * 128;
+    const uint32_t sa_hi = smem_u32(ahi), sa_lo = smem_u32(alo), sb = smem_u32(b);
 #pragma unroll
     for (int t = 0; t < 9; ++t) {
         const uint32_t oa = (uint32_t)((t / 3) * W + (t % 3)) * 16, ob = 2u * t * lbo_b;
-        umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, t > 0);
+        const uint64_t a_hi = umma_desc(sa_hi + oa, lbo_a, 128), b_hi = umma_desc(sb + ob, lbo_b, 128);
+        umma_tf32(d_tmem, a_hi, b_hi, stacked ? idesc2 : idesc, t > 0);
         if (split) {
-            umma_tf32(d_tmem, umma_desc(sa_hi + oa, lbo_a, 128), umma_desc(sb_lo + ob, lbo_b, 128), idesc, 1);
-            umma_tf32(d_tmem, umma_desc(sa_lo + oa, lbo_a, 128), umma_desc(sb_hi + ob, lbo_b, 128), idesc, 1);
+            if (!stacked) umma_tf32(d_tmem, a_hi, umma_desc(sb + ob + lo_rows, lbo_b, 128), idesc, 1);
+            umma_tf32(d_tmem, umma_desc(sa_lo + oa, lbo_a, 128), b_hi, idesc, 1);
         }
     }
     umma_commit(bar);

@@ -57,8 +57,9 @@ CONV_SHAPES = [
     (1, 8, 128, 128, 64),   # one full sample of the chain's input
     (3, 3, 7, 9, 16),       # K = 27 padded to 32, one partial tile
     (2, 1, 5, 5, 32),       # K = 9 padded to 16
-    (1, 8, 130, 131, 128),  # Cout = 128, ragged last tile
+    (1, 8, 130, 131, 128),  # Cout = 128, ragged last tile (three MMAs per tap)
     (5, 4, 12, 3, 48),      # OW = 1
+    (2, 8, 14, 18, 80),     # Cout = 80: three MMAs per tap, 128 accumulator columns
 ]
 
 
@@ -105,6 +106,7 @@ CHAIN_CASES = [
     (2, 8, 12, 14, 64, 64),     # 1 channel per group
     (2, 8, 12, 14, 64, 4),      # 16 channels per group
     (1, 8, 20, 7, 48, 6),       # 8 channels per group, Cout = 48
+    (1, 8, 20, 22, 128, 16),    # Cout = 128: the unstacked products in every epilogue
 ]
 
 
