@@ -57,10 +57,14 @@ enum ConvMode { kConvWriteY = 0, kConvStats = 1, kConvApplyLse = 2, kConvWriteYS
 
 constexpr int kConvMaxSlots = 4;
 
+// Row stride (float2) of the statistics scratch [G][pixel]: 8 past the tile's
+// 128 pixels, so that the rows of neighbouring groups start 16 banks apart.
+constexpr int kConvWsmStride = kConvTileM + 8;
+
 // Bytes of one slot: the window's hi and lo parts, or the statistics scratch
-// [G][128] float2 when that is larger (it reuses the same space).
+// [G][kConvWsmStride] float2 when that is larger (it reuses the same space).
 __host__ __device__ static inline size_t conv_slot_bytes(int S, int G) {
-    const size_t win = (size_t)S * 16 * 2 * 2, st = (size_t)G * kConvTileM * 8;
+    const size_t win = (size_t)S * 16 * 2 * 2, st = (size_t)G * kConvWsmStride * 8;
     return win > st ? win : st;
 }
 
@@ -220,8 +224,8 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
                     float m2 = 0.f;
 #pragma unroll
                     for (int j = 0; j < CPG; ++j) m2 = fmaf(v[lo + j] - mean, v[lo + j] - mean, m2);
-                    wsm[((c0 + lo) / CPG) * kConvTileM + wtid] = valid ? make_float2(mean, m2)
-                                                                       : make_float2(0.f, -1.f);
+                    wsm[((c0 + lo) / CPG) * kConvWsmStride + wtid] = valid ? make_float2(mean, m2)
+                                                                           : make_float2(0.f, -1.f);
                 }
             }
         }
@@ -229,26 +233,45 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
             if (valid) a.out[n * ohw + p] = ms_lse(st);
         }
         if constexpr (STATS) {
-            // merge over the tile's pixels: tpg threads per group, each a strided
-            // share of the pixels, then shuffles within the tpg-lane block
+            // merge over the tile's pixels, tpg threads per group, each a strided share
+            // of the pixels, reduced by shuffles within the tpg-lane block.  Every
+            // valid pixel holds CPG values, so the merge is exact in two passes: the
+            // group's mean is the mean of the pixel means, and its M2 the sum of the
+            // pixel M2s plus CPG (mean_p - mean)^2 per pixel.
             named_bar_sync(bar_id, kConvTileM);
             const int G = a.G;
             int tpg = 1;
             while (tpg * 2 * G <= kConvTileM && tpg < 32) tpg *= 2;
             const int g = wtid / tpg, j = wtid - g * tpg;
-            Welford w{0.f, 0.f, 0.f};
+            const float2* const row = wsm + (g < G ? g : 0) * kConvWsmStride;
+            float cnt = 0.f, s1 = 0.f;
             if (g < G) {
                 for (int m = j; m < kConvTileM; m += tpg) {
-                    const float2 qv = wsm[g * kConvTileM + m];
-                    if (qv.y >= 0.f) w = wf_merge(w, Welford{(float)CPG, qv.x, qv.y});  // M2 < 0 marks no pixel
+                    const float2 qv = row[m];
+                    if (!(qv.y < 0.f)) {  // M2 < 0 marks no pixel; a NaN pixel counts
+                        cnt += 1.f;
+                        s1 += qv.x;
+                    }
                 }
             }
             for (int o = 1; o < tpg; o <<= 1) {
-                const Welford other = wf_shfl_xor(w, o);
-                w = wf_merge(w, other);
+                cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
             }
+            const float mean = cnt > 0.f ? s1 / cnt : 0.f;
+            float m2 = 0.f;
+            if (g < G) {
+                for (int m = j; m < kConvTileM; m += tpg) {
+                    const float2 qv = row[m];
+                    if (!(qv.y < 0.f)) {
+                        const float d = qv.x - mean;
+                        m2 += fmaf((float)CPG * d, d, qv.y);
+                    }
+                }
+            }
+            for (int o = 1; o < tpg; o <<= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
             if (g < G && j == 0)
-                a.partials[(n * a.tiles + (q0 / kConvTileM)) * G + g] = make_float4(w.n, w.mean, w.m2, 0.f);
+                a.partials[(n * a.tiles + (q0 / kConvTileM)) * G + g] = make_float4(cnt * CPG, mean, m2, 0.f);
         }
         tc_fence_before();
         named_bar_sync(bar_id, kConvTileM);  // this slot is done reading D and its window / scratch

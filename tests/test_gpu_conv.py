@@ -129,6 +129,30 @@ def test_conv_chain_parity(lib, N, Cin, H, W, Cout, G, chain, monkeypatch):
     assert_parity(got, ref, f"conv chain {N, Cin, H, W, Cout, G}")
 
 
+def test_conv2d_nan_input(lib):
+    """A NaN input pixel makes NaN exactly the outputs whose window holds it, in every channel."""
+    inp = _inputs(2, 8, 14, 16, 64)
+    inp["x"] = inp["x"].clone()
+    inp["x"][0, 3, 5, 7] = float("nan")
+    got = _conv(lib, inp)
+    assert int(torch.isnan(got).sum()) == 9 * 64
+    assert_parity(got, oracle.conv2d(inp["x"], inp["w"], inp["bias"]), "conv2d with a NaN input")
+
+
+@pytest.mark.parametrize("chain", ["1", "2"], ids=["y-round-trip", "y-free"])
+def test_conv_chain_nan_input(lib, chain, monkeypatch):
+    """A NaN in one sample's input reaches every group mean of that sample, so the
+    whole sample's output is NaN; the other sample is untouched."""
+    monkeypatch.setenv("LSE_CONV_CHAIN", chain)
+    inp = _inputs(2, 8, 14, 16, 64)
+    inp["x"] = inp["x"].clone()
+    inp["x"][0, 3, 5, 7] = float("nan")
+    got = _chain(lib, inp, 16)
+    assert bool(torch.isnan(got[0]).all()) and not bool(torch.isnan(got[1]).any())
+    ref = oracle.conv_gn_act_lse(inp["x"], inp["w"], inp["bias"], inp["gamma"], inp["beta"], 16, 1e-5)
+    assert_parity(got, ref, "conv chain with a NaN input")
+
+
 def test_conv_chain_other_cin_is_two_calls(lib):
     """Cin other than the layer's 8 is not fused: the call reports it, and the two
     calls it stands for give the chain."""
