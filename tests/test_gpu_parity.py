@@ -303,6 +303,30 @@ def test_gn_act_lse_variants(lib, env, cfg, N, C, H, W, G):
     assert_parity(got, ref, f"gn {cfg} {N,C,H,W,G}")
 
 
+def _non_finite_gn_input():
+    """Four samples of y[., 16, 6, 7] (4 channels per group at G = 4): a NaN in sample 0
+    group 1, +inf in sample 1 group 0, -inf in sample 2 group 2, sample 3 finite."""
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(4, 16, 6, 7))
+    y = inp["y"].clone()
+    y[0, 5, 2, 3] = float("nan")
+    y[1, 1, 0, 0] = float("inf")
+    y[2, 10, 5, 6] = float("-inf")
+    return y, inp["gamma"], inp["beta"]
+
+
+@pytest.mark.parametrize("variant", ["0", "1", "2", "3"])
+def test_gn_act_lse_non_finite(lib, env, variant):
+    """A non-finite value makes its group's mean or variance NaN, so every channel of that
+    group is NaN at every pixel and the sample's channel lse is NaN everywhere; the
+    finite sample is unaffected (the oracle's plain definition, variance over all values)."""
+    env.setenv("LSE_GN_VARIANT", variant)
+    y, gamma, beta = _non_finite_gn_input()
+    got = lib.gn_act_lse_forward(y.to(DEV), gamma.to(DEV), beta.to(DEV), 4, 1e-5).cpu()
+    assert all(bool(torch.isnan(got[n]).all()) for n in range(3))
+    assert not bool(torch.isnan(got[3]).any())
+    assert_parity(got, oracle.gn_act_lse(y, gamma, beta, 4, 1e-5), f"non-finite y, variant {variant}")
+
+
 def test_gn_act_lse_wide_range(lib):
     """Large gamma and shifted data: z spans about [-60, 60] (tanh saturates),
     a non-zero mean exercises the statistics."""

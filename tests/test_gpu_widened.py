@@ -218,6 +218,25 @@ def test_gn_elementwise_misaligned(lib, fn):
                   f"{fn} misaligned")
 
 
+@pytest.mark.parametrize("variant", ["0", "2", "3"])
+@pytest.mark.parametrize("fn", ["group_norm", "gn_act_residual"])
+def test_gn_elementwise_non_finite(lib, env, fn, variant):
+    """NaN, +inf or -inf in a group makes exactly that group NaN (its mean or variance is
+    NaN); the other groups and samples match the oracle."""
+    env.setenv("LSE_GN_VARIANT", variant)
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(4, 16, 6, 7))
+    y = inp["y"].clone()
+    y[0, 5, 2, 3] = float("nan")
+    y[1, 1, 0, 0] = float("inf")
+    y[2, 10, 5, 6] = float("-inf")
+    inp["y"] = y
+    got = _gn(lib, fn, inp, 4)
+    nan = torch.isnan(got)
+    assert int(nan.sum()) == 3 * 4 * 42
+    assert bool(nan[0, 4:8].all() and nan[1, 0:4].all() and nan[2, 8:12].all())
+    assert_parity(got, getattr(oracle, fn)(y, inp["gamma"], inp["beta"], 4, 1e-5), f"{fn} non-finite y")
+
+
 @pytest.mark.parametrize("cfg", [{"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "5", "LSE_GN_LAG": "0"},
                                  {"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "16", "LSE_GN_LAG": "100",
                                   "LSE_GN_CTAS_PER_SM": "1"},

@@ -14,6 +14,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import synth
 from tests.parity import assert_parity
 
@@ -49,6 +50,18 @@ def test_noalloc_matches_allocating_entry_point():
         assert rc == 0, L.lse_status_string(rc)
         torch.cuda.synchronize()
         assert_parity(got.cpu(), ref.cpu().double().numpy(), f"noalloc vs gn_act_lse {N,C,H,W,G}")
+
+    # non-finite values: NaN / +inf / -inf in one group of samples 0 / 1 / 2 make those
+    # samples NaN, as in the oracle; sample 3 stays finite
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(4, 16, 6, 7))
+    y = inp["y"].clone()
+    y[0, 5, 2, 3], y[1, 1, 0, 0], y[2, 10, 5, 6] = float("nan"), float("inf"), float("-inf")
+    yd, gd, bd = y.to(DEV), inp["gamma"].to(DEV), inp["beta"].to(DEV)
+    got = torch.empty(4, 1, 6, 7, device=DEV)
+    rc = lib.gn_act_lse_noalloc(_p(yd), _p(gd), _p(bd), _p(got), 4, 16, 42, 4, 1e-5, stream)
+    assert rc == 0, L.lse_status_string(rc)
+    torch.cuda.synchronize()
+    assert_parity(got.cpu(), oracle.gn_act_lse(y, inp["gamma"], inp["beta"], 4, 1e-5), "noalloc, non-finite y")
 
     # beyond the fixed scratch (N * G > 65536): rejected before any launch
     big = torch.empty(4, device=DEV)
