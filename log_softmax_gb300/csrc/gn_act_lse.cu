@@ -186,8 +186,11 @@ __global__ void __launch_bounds__(128) gn_apply_kernel(const float* __restrict__
     const int cpg = C / G;
     int64_t cur_n = -1;
     for (int64_t b = blockIdx.x; b < N * tiles; b += gridDim.x) {
-        const int64_t n = b / tiles;
-        const int64_t tile = b - n * tiles;
+        // samples last to first: the kernel before this one (the statistics pass or
+        // the convolution) went first to last, so the last samples' y is still in L2
+        const int64_t k = b / tiles;
+        const int64_t n = N - 1 - k;
+        const int64_t tile = b - k * tiles;
         if (n != cur_n) {  // uniform across the block
             __syncthreads();
             for (int c = tid; c < C; c += T) {
