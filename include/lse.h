@@ -212,6 +212,11 @@ lse_status_t conv_gn_act_lse(const float* x, const float* w, const float* b, con
  *   gamma  [C], beta [C] fp32, device, read only.
  *   out    [N * HW] fp32, device, written.
  *   N >= 0, HW >= 0, 1 <= C <= 8192, G >= 1, C % G == 0; eps >= 0 and finite.
+ *   - Special values: a NaN, +inf or -inf anywhere in a group makes that
+ *     group's mean or variance NaN, hence every z of the group NaN; since the
+ *     lse spans all channels, the whole sample's output is then NaN (the
+ *     statistics are taken over all of the group's values, as defined above).
+ *     group_norm and gn_act_residual give NaN for exactly that group.
  * The per-(n, g) statistics and a work counter need 16*N*G + 4*N + 32 bytes of
  * scratch.  The library takes them, stream-ordered, from a memory pool it owns
  * on the current device
