@@ -37,9 +37,10 @@
  *   - Accuracy: fp32 storage and accumulation; results agree with a double
  *     precision evaluation within |err| <= 2e-5 + 1e-6 * |ref|.
  *   - CUDA graphs: every entry point on device pointers can be captured into
- *     a graph once one call has run on the device (the first call does a
- *     one-time set-up that must not happen inside a capture).  Scratch then
- *     becomes graph memory nodes, so replays are independent.
+ *     a graph once the same call (same entry point, sizes and alignment) has
+ *     run on the device outside a capture: first calls create the library's
+ *     memory pool and load kernels, which must not happen inside a capture.
+ *     Scratch then becomes graph memory nodes, so replays are independent.
  *     log_softmax_lastdim_host (its own copy streams) and lse_device_status
  *     (it synchronises) are not capturable.
  */
