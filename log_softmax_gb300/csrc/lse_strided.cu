@@ -12,10 +12,13 @@
 //
 // With LSM set the same kernel writes log_softmax over the strided axis
 // instead of the lse (out has x's shape): the block publishes its columns'
-// lse in shared memory, then walks its tile a second time and writes
-// x - lse.  The first walk marks its lines evict-last in L2 and the second
-// evict-first, so the second walk is served from L2 while the tiles resident
-// at once fit there; x is read from HBM once and out written once.
+// lse in shared memory and writes x - lse.  When R = CH * TY each thread's
+// values are one load batch, kept in registers from the reduction to the
+// write (ONE: the tile is read once).  Otherwise the block walks its tile a
+// second time: the first walk marks its lines evict-last in L2 and the
+// second evict-first, so the second walk is served from L2 while the tiles
+// resident at once fit there.  Either way x is read from HBM once and out
+// written once.
 #include <algorithm>
 
 #include "common.cuh"
@@ -33,7 +36,10 @@ __device__ __forceinline__ void load_cols(const float* p, float (&v)[VEC], uint6
     }
 }
 
-template <int VEC, int CH, bool LSM>
+// ONE (with LSM, for R = CH * TY): a thread's rows ty, ty + TY, ... of its
+// columns are one load batch, kept in registers for the write, so the tile is
+// read once (no second walk through L2).
+template <int VEC, int CH, bool LSM, bool ONE = false>
 __global__ void __launch_bounds__(256) lse_strided_kernel(const float* __restrict__ x,
                                                           float* __restrict__ out, int64_t outer,
                                                           int64_t R, int64_t inner, int64_t tiles) {
@@ -51,7 +57,25 @@ __global__ void __launch_bounds__(256) lse_strided_kernel(const float* __restric
         MS st[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; ++j) st[j] = ms_empty();
-        if (valid) {
+        static_assert(!ONE || LSM, "the one-walk form writes log_softmax");
+        constexpr bool one_walk = ONE;
+        float keep_v[ONE ? VEC : 1][ONE ? CH : 1];
+        if constexpr (ONE) {
+            if (valid) {
+                const float* base = x + o * R * inner + c0 + (int64_t)ty * inner;
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    float w[VEC];
+                    load_cols<VEC>(base + (int64_t)k * TY * inner, w, 0, false);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) keep_v[ONE ? j : 0][ONE ? k : 0] = w[j];
+                }
+                if constexpr (ONE) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) ms_fold<CH>(st[j], keep_v[j]);
+                }
+            }
+        } else if (valid) {
             const float* base = x + o * R * inner + c0;
             int64_t r = ty;
             const int64_t step = (int64_t)CH * TY;
@@ -105,7 +129,22 @@ __global__ void __launch_bounds__(256) lse_strided_kernel(const float* __restric
                 for (int j = 0; j < VEC; ++j) lse_s[tx * VEC + j] = ms_lse(st[j]);
             }
             __syncthreads();
-            if (valid) {
+            if (valid && one_walk) {  // constant: one of the two branches is compiled
+                float l[VEC];
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) l[j] = lse_s[tx * VEC + j];
+                float* dst = out + o * R * inner + c0 + (int64_t)ty * inner;
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    const int kk = ONE ? k : 0;
+                    if constexpr (VEC == 4)
+                        st_stream_f4(dst + (int64_t)k * TY * inner,
+                                     make_float4(keep_v[0][kk] - l[0], keep_v[ONE ? 1 : 0][kk] - l[1],
+                                                 keep_v[ONE ? 2 : 0][kk] - l[2], keep_v[ONE ? 3 : 0][kk] - l[3]));
+                    else
+                        st_stream_f1(dst + (int64_t)k * TY * inner, keep_v[0][kk] - l[0]);
+                }
+            } else if (valid) {
                 float l[VEC];
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) l[j] = lse_s[tx * VEC + j];
@@ -151,6 +190,10 @@ static int pow2_ceil(int64_t v) {
 template <bool LSM>
 static void strided_go(bool vec4, int CH, unsigned grid, dim3 block, const float* x, float* out, int64_t outer,
                        int64_t R, int64_t inner, int64_t tiles, cudaStream_t stream) {
+    if (LSM && vec4 && CH == 8 && R == 8 * (int64_t)block.y && env_int("LSE_STRIDED_ONE_WALK", 1)) {
+        lse_strided_kernel<4, 8, true, true><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);
+        return;
+    }
     if (vec4) {
         if (CH == 8)
             lse_strided_kernel<4, 8, LSM><<<grid, block, 0, stream>>>(x, out, outer, R, inner, tiles);

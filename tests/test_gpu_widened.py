@@ -146,6 +146,18 @@ def test_log_softmax_dim_parity(lib, outer, R, inner, misalign):
     assert_parity(got, oracle.log_softmax_dim(x, outer, R, inner), f"lsm dim {outer,R,inner}")
 
 
+@pytest.mark.parametrize("one_walk", ["0", "1"], ids=["two-walks", "one-walk"])
+@pytest.mark.parametrize("outer,R,inner", [(1, 8, 1000), (3, 16, 260), (1, 32, 4096), (2, 64, 12),
+                                           (2, 32, 40000)])
+def test_log_softmax_dim_walks(lib, env, one_walk, outer, R, inner):
+    """R = 8 x the thread rows: the tile kept in registers (one walk) or walked twice
+    through L2; both give the oracle's result, ragged inner tiles included."""
+    env.setenv("LSE_STRIDED_ONE_WALK", one_walk)
+    x = synth.uniform((outer, R, inner), seed=outer * 5 + R + inner, lo=-20, hi=20)
+    got = _lsm_dim(lib, x, outer, R, inner, False)
+    assert_parity(got, oracle.log_softmax_dim(x, outer, R, inner), f"lsm dim {outer, R, inner} walks {one_walk}")
+
+
 def test_log_softmax_dim_special_values(lib):
     inf, nan = float("inf"), float("nan")
     cols = [[1.0, nan, 2.0, 0.0], [nan, inf, 0.0, 1.0], [inf, 1.0, -inf, 0.0],
