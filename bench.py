@@ -573,6 +573,48 @@ def run_ours(args, w: synth.Workload):
     return 0
 
 
+def host_link(host_in, host_out, dev, max_bytes=1 << 30):
+    """Copy-engine bandwidth of this process's host link with its own pinned buffers:
+    host to device, device to host, and both at once (two streams), GB/s."""
+    src = next(iter(host_in.values())).view(-1)
+    dst = host_out.view(-1)
+    n = int(min(src.numel(), dst.numel(), max_bytes // 4))
+    if n == 0:
+        return None
+    src, dst = src[:n], dst[:n]
+    a = torch.empty(n, device=dev)
+    b = torch.empty(n, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        fn()
+        torch.cuda.synchronize(dev)
+        return time.perf_counter() - t0
+
+    def both():
+        with torch.cuda.stream(s1):
+            b.copy_(src, non_blocking=True)
+        with torch.cuda.stream(s2):
+            dst.copy_(a, non_blocking=True)
+
+    a.copy_(src, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    h2d = n * 4 / timed(lambda: a.copy_(src, non_blocking=True)) / 1e9
+    d2h = n * 4 / timed(lambda: dst.copy_(a, non_blocking=True)) / 1e9
+    bi = 2 * n * 4 / timed(both) / 1e9
+    return {"h2d_gbs": round(h2d, 1), "d2h_gbs": round(d2h, 1), "both_gbs": round(bi, 1), "bytes_each": n * 4}
+
+
+def e2e_ceiling(nbytes, h2d_bytes, d2h_bytes, link):
+    """The e2e value (algorithmic bytes per second, GB/s) if every step took only the
+    time its copies need on `link`: one direction at a time, or both at once."""
+    t = max(h2d_bytes / (link["h2d_gbs"] * 1e9), d2h_bytes / (link["d2h_gbs"] * 1e9),
+            (h2d_bytes + d2h_bytes) / (link["both_gbs"] * 1e9))
+    return nbytes / t / 1e9 if t > 0 else None
+
+
 def run_e2e(L, w: synth.Workload, inputs, args, dev, world):
     """Same metric through the public Python API with pinned host buffers: each step
     copies its input host->device, runs the call and copies the result back."""
@@ -614,10 +656,19 @@ def run_e2e(L, w: synth.Workload, inputs, args, dev, world):
     total = sum_over_ranks(float(nbytes * steps), world, dev)
     h2d = sum(t.numel() * 4 for t in host_in.values())
     d2h = host_out.numel() * 4
-    return {"value": round(total / dt / 1e9, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps,
-            "note": "pinned host buffers; every step copies its input in and its result out "
-                    "(log_softmax: chunked pipeline overlapping both copies with the call)"}
+    value = round(total / dt / 1e9, 3)
+    out = {"value": value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": steps,
+           "note": "pinned host buffers; every step copies its input in and its result out "
+                   "(log_softmax: chunked pipeline overlapping both copies with the call)"}
+    link = host_link(host_in, host_out, dev)
+    if link is not None:
+        ceil = e2e_ceiling(nbytes, h2d, d2h, link)
+        out["host_link"] = link
+        if ceil:
+            out["link_ceiling"] = round(ceil, 1)
+            out["frac_of_link"] = round(value / world / ceil, 4)
+    return out
 
 
 def main(argv=None):
