@@ -327,6 +327,25 @@ def test_gn_act_lse_non_finite(lib, env, variant):
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, 4, 1e-5), f"non-finite y, variant {variant}")
 
 
+@pytest.mark.parametrize("variant", ["0", "1", "2", "3"])
+@pytest.mark.parametrize("N,H,W,G", [(2, 3, 4, 512), (1, 2, 2, 8192), (2, 3, 3, 64)])
+def test_gn_max_channels(lib, env, variant, N, H, W, G):
+    """C = 8192, the largest accepted: the per-channel table fills 128 KB of shared memory
+    in every kernel variant (HW = 9: the scalar kernels)."""
+    env.setenv("LSE_GN_VARIANT", variant)
+    C = 8192
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))
+    y, g, b = (inp[k].to(DEV) for k in ("y", "gamma", "beta"))
+    got = lib.gn_act_lse_forward(y, g, b, G, 1e-5).cpu()
+    assert_parity(got, oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], G, 1e-5), f"C=8192 G={G} v{variant}")
+    for fn in ("group_norm", "gn_act_residual"):
+        out = torch.full((N, C, H, W), float("nan"), device=DEV)
+        getattr(lib, fn)(y, g, b, out, N, C, H * W, G, 1e-5)
+        torch.cuda.synchronize()
+        assert_parity(out.cpu(), getattr(oracle, fn)(inp["y"], inp["gamma"], inp["beta"], G, 1e-5),
+                      f"{fn} C=8192 G={G} v{variant}")
+
+
 def test_gn_act_lse_wide_range(lib):
     """Large gamma and shifted data: z spans about [-60, 60] (tanh saturates),
     a non-zero mean exercises the statistics."""
