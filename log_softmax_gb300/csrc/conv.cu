@@ -361,11 +361,16 @@ static cudaError_t conv_go(const DeviceInfo& dev, const ConvArgs& a0, cudaStream
     // raw windows by bulk copies when every plane starts 16-byte aligned
     a.tma = ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0 && ((int64_t)a.H * a.W) % 4 == 0 &&
              env_int("LSE_CONV_TMA", 1) != 0) ? 1 : 0;
-    const size_t wbytes = conv_weight_bytes(a.cout),
-                 sbytes = conv_slot_bytes(a.S, (MODE == kConvStats || MODE == kConvWriteYStats) ? a.G : 0) +
-                          (a.tma ? conv_raw_bytes(a.S) : 0) +
-                          (MODE == kConvApplyLse ? conv_tab_bytes(a.cout) : 0);
+    const size_t wbytes = conv_weight_bytes(a.cout);
     const size_t budget = (size_t)dev.max_smem_optin - 1024;
+    auto slot_bytes = [&]() {
+        return conv_slot_bytes(a.S, (MODE == kConvStats || MODE == kConvWriteYStats) ? a.G : 0) +
+               (a.tma ? conv_raw_bytes(a.S) : 0) + (MODE == kConvApplyLse ? conv_tab_bytes(a.cout) : 0);
+    };
+    // wide rows: when the raw window buffer of the bulk-copy path does not fit
+    // beside one slot's window, load the window directly instead
+    if (a.tma && wbytes + slot_bytes() > budget) a.tma = 0;
+    const size_t sbytes = slot_bytes();
     if (wbytes + sbytes > budget) return cudaErrorNotSupported;
     a.slots = (int)std::min<size_t>({(size_t)kConvMaxSlots, (budget - wbytes) / sbytes,
                                      (size_t)(512 / conv_tmem_cols(a.cout))});

@@ -60,6 +60,9 @@ CONV_SHAPES = [
     (1, 8, 130, 131, 128),  # Cout = 128, ragged last tile (three MMAs per tap)
     (5, 4, 12, 3, 48),      # OW = 1
     (2, 8, 14, 18, 80),     # Cout = 80: three MMAs per tap, 128 accumulator columns
+    (1, 8, 5, 1024, 64),    # W = 1024, the widest accepted: the window is loaded directly
+    (1, 8, 4, 1024, 128),   # the same with the largest Cout
+    (1, 8, 6, 900, 64),     # the widest that keeps the bulk-copy window at Cout = 64
 ]
 
 
@@ -107,6 +110,7 @@ CHAIN_CASES = [
     (2, 8, 12, 14, 64, 4),      # 16 channels per group
     (1, 8, 20, 7, 48, 6),       # 8 channels per group, Cout = 48
     (1, 8, 20, 22, 128, 16),    # Cout = 128: the unstacked products in every epilogue
+    (1, 8, 5, 1024, 64, 16),    # W = 1024
 ]
 
 
