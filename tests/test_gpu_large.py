@@ -68,6 +68,26 @@ def test_rows_past_2_31(lib, fn, rows, cols):
     del x, out
 
 
+@pytest.mark.parametrize("fn", ["log_softmax_lastdim", "softmax_lastdim", "row_lse"])
+def test_rows_of_40m(lib, fn):
+    """Rows of 40 million floats (160 MB), far past what shared memory can stage: the
+    streaming row kernels, compared with the oracle element by element."""
+    rows, cols = 2, 40_000_000
+    x = synth.make_inputs("log_softmax_4096x393216", shape=(rows, cols), device=DEV)["x"]
+    xc = x.cpu()
+    if fn == "row_lse":
+        out = torch.empty(rows, device=DEV)
+        lib.lse_reduce(x, out, rows, cols, 1)
+        ref = oracle.lse_reduce(xc.view(rows, cols, 1), rows, cols, 1)
+    else:
+        out = torch.empty_like(x)
+        getattr(lib, fn)(x, out, rows, cols)
+        ref = (oracle.log_softmax if fn == "log_softmax_lastdim" else oracle.softmax)(xc)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().view(ref.shape), ref, f"{fn} rows of {cols}")
+    del x, out
+
+
 @pytest.mark.parametrize("outer,R,inner", [(1, 4, 540_000_000), (65_600, 8, 4096)])
 def test_lse_reduce_past_2_31(lib, outer, R, inner):
     assert outer * R * inner > BIG
