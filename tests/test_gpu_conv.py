@@ -63,6 +63,8 @@ CONV_SHAPES = [
     (1, 8, 5, 1024, 64),    # W = 1024, the widest accepted: the window is loaded directly
     (1, 8, 4, 1024, 128),   # the same with the largest Cout
     (1, 8, 6, 900, 64),     # the widest that keeps the bulk-copy window at Cout = 64
+    (2, 8, 3, 40, 32),      # H = 3: one output row
+    (3, 5, 3, 3, 16),       # a 1 x 1 output per sample
 ]
 
 
