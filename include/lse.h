@@ -43,6 +43,33 @@
  *     Scratch then becomes graph memory nodes, so replays are independent.
  *     log_softmax_lastdim_host (its own copy streams) and lse_device_status
  *     (it synchronises) are not capturable.
+ *
+ * Environment switches (read at each call; none is needed, every default is
+ * the measured best on GB300, and every setting gives the same results within
+ * the tolerance above):
+ *   - Kernel choice: LSE_LSM_VARIANT (rows: 1 registers, 2 cluster shared
+ *     memory, 3 streaming, 4 lock-step group, 5 group with an L2 re-read,
+ *     6 warp-specialised group; default by shape), LSE_GN_VARIANT (GroupNorm
+ *     forms: 1 statistics kernel then apply kernel, 2 work queue with
+ *     per-thread loads, 3 work queue with bulk-copy staging; default 2 for
+ *     gn_act_lse, 3 for group_norm and gn_act_residual), LSE_CONV_CHAIN
+ *     (conv_gn_act_lse: 1 y written and read back, 2 y never in memory;
+ *     default 1), LSE_CONV_TMA (0: convolution windows loaded directly),
+ *     LSE_STRIDED_ONE_WALK (0: the strided log_softmax always walks a tile
+ *     twice).
+ *   - Tuning: LSE_WS_GROUP / LSE_WS_NB / LSE_WS_FW / LSE_WS_SW (warp-
+ *     specialised rows: CTAs per row, buffers, fold and store warps),
+ *     LSE_LSM_CLUSTER / LSE_LSM_GROUP / LSE_LSM_THREADS / LSE_LSM_NBUF /
+ *     LSE_LSM_CHUNK, LSE_L2_GROUP / LSE_L2_THREADS, LSE_STREAM_CLUSTER (the
+ *     other row kernels), LSE_GN_THREADS / LSE_GN_PARTS / LSE_GN_LAG /
+ *     LSE_GN_CTAS_PER_SM and LSE_GNT_SLOTS / LSE_GNT_LAG / LSE_GNT_CTAS_PER_SM
+ *     (the two GroupNorm work queues), LSE_HOST_CHUNK_MB (host pipeline chunk).
+ *   - LSE_VERBOSE=1 prints each launch's plan on stderr.
+ *   - Test hooks, not for production: LSE_TEST_FAIL_ALLOC=1 makes every
+ *     scratch allocation fail (the call returns LSE_ERR_CUDA and enqueues
+ *     nothing); LSE_TEST_UNREACHABLE_WAIT=1 makes the GroupNorm work queue
+ *     wait for a statistics part that never comes, so its bounded waits run
+ *     out (~1 s) and lse_device_status reports LSE_ERR_TIMEOUT.
  */
 #ifndef LSE_H
 #define LSE_H
