@@ -50,9 +50,10 @@
  *   - Kernel choice: LSE_LSM_VARIANT (rows: 1 registers, 2 cluster shared
  *     memory, 3 streaming, 4 lock-step group, 5 group with an L2 re-read,
  *     6 warp-specialised group; default by shape), LSE_GN_VARIANT (GroupNorm
- *     forms: 1 statistics kernel then apply kernel, 2 work queue with
- *     per-thread loads, 3 work queue with bulk-copy staging; default 2 for
- *     gn_act_lse, 3 for group_norm and gn_act_residual), LSE_CONV_CHAIN
+ *     forms: 1 statistics kernel then apply kernel (gn_act_lse only), 2 work
+ *     queue with per-thread loads, 3 work queue with bulk-copy staging;
+ *     default 2 for gn_act_lse, 3 for group_norm and gn_act_residual),
+ *     LSE_CONV_CHAIN
  *     (conv_gn_act_lse: 1 y written and read back, 2 y never in memory;
  *     default 1), LSE_CONV_TMA (0: convolution windows loaded directly),
  *     LSE_STRIDED_ONE_WALK (0: the strided log_softmax always walks a tile
