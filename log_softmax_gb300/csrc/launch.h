@@ -81,10 +81,10 @@ cudaError_t launch_gn_apply(const DeviceInfo& dev, const float* y, const float* 
 
 // Form 3 in one cooperative kernel: statistics parts and apply tiles of the
 // samples claimed from one work queue, each sample's second read close behind
-// its first so that it hits L2.  Scratch: gn_fused_scratch_bytes(N, G).
+// its first so that it hits L2.  Scratch: gn_fused_scratch_bytes(N, G, out_kind).
 // out_kind 0 writes the channel lse (N x HW); 1 the GroupNorm output and 2 the
 // chain before the lse, y + hardswish(tanh(GroupNorm(y))) (both N x C x HW).
-size_t gn_fused_scratch_bytes(int64_t N, int64_t G);
+size_t gn_fused_scratch_bytes(int64_t N, int64_t G, int out_kind);
 cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const float* gamma,
                                     const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
                                     int64_t G, float eps, void* scratch, cudaStream_t stream,

@@ -268,7 +268,7 @@ lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, flo
     const bool want_tma = variant == 3 || (variant != 2 && out_kind != 0);
     const bool tma = want_tma && gn_tma_applies(s->info, y, out, C, HW);
     void* scratch = nullptr;
-    cudaError_t e = pool_alloc(&scratch, tma ? gn_tma_scratch_bytes(N, G) : gn_fused_scratch_bytes(N, G),
+    cudaError_t e = pool_alloc(&scratch, tma ? gn_tma_scratch_bytes(N, G) : gn_fused_scratch_bytes(N, G, out_kind),
                                             pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     if (tma)
