@@ -57,7 +57,7 @@ def algorithmic_bytes(w: synth.Workload) -> int:
         C = w.shape[1]
         return 4 * (2 * w.numel + 2 * C)
     if w.op == "conv_gn_act_lse":
-        # x once, y written once by the conv and read once by the apply pass, out;
+        # x once, y written once by the conv and read once by the GroupNorm pass, out;
         # weights, bias, gamma, beta
         N, Cin, H, W = w.shape
         Cout = w.params["Cout"]
@@ -77,7 +77,7 @@ LAUNCHES = {
     "log_softmax_dim0": ["lse_strided_kernel"],
     "group_norm": ["gn_tma_kernel"],
     "gn_act_residual": ["gn_tma_kernel"],
-    "conv_gn_act_lse": ["conv2d_tc_kernel", "gn_tile_merge_kernel", "gn_apply_kernel"],
+    "conv_gn_act_lse": ["conv2d_tc_kernel", "gn_fused_kernel"],
 }
 
 

@@ -53,9 +53,10 @@
  *     forms: 1 statistics kernel then apply kernel (gn_act_lse only), 2 work
  *     queue with per-thread loads, 3 work queue with bulk-copy staging;
  *     default 2 for gn_act_lse, 3 for group_norm and gn_act_residual),
- *     LSE_CONV_CHAIN
- *     (conv_gn_act_lse: 1 y written and read back, 2 y never in memory;
- *     default 1), LSE_CONV_TMA (0: convolution windows loaded directly),
+ *     LSE_CONV_CHAIN (conv_gn_act_lse: 1 y and its tiles' statistics from
+ *     the convolution's epilogue, then merge and apply; 2 y never in memory;
+ *     3 y, then the GroupNorm work queue over it; default 3), LSE_CONV_TMA
+ *     (0: convolution windows loaded directly),
  *     LSE_STRIDED_ONE_WALK (0: the strided log_softmax always walks a tile
  *     twice).
  *   - Tuning: LSE_WS_GROUP / LSE_WS_NB / LSE_WS_FW / LSE_WS_SW (warp-
@@ -222,14 +223,15 @@ lse_status_t conv2d_3x3(const float* x, const float* w, const float* b, float* y
  *   in {1, 2, 4, 8, 16} and G <= 64 (else LSE_ERR_UNSUPPORTED); eps >= 0 and
  *   finite; the
  *   conv2d_3x3 shape rules.  Other shapes: conv2d_3x3 then gn_act_lse.
- * The convolution's epilogue writes y and the Welford partials of every
- * (sample, 128-pixel tile, group), so the statistics never re-read y; after
- * they are merged the apply pass reads y once.  Scratch (y itself, about
- * N*Cout*(H-2)*(W-2)*4 bytes, plus the partials) comes from the library's pool
- * on `stream`.  (LSE_CONV_CHAIN=2 selects a form where y never reaches memory:
- * the convolution runs twice and the second pass finishes the chain from the
- * tensor-core accumulators; it is slower on GB300 while the convolution is
- * bound by its tensor work.)
+ * The convolution writes y, then gn_act_lse's one-kernel work queue runs over
+ * it, walking the samples last to first so that its first reads find the
+ * convolution's last samples in L2.  Scratch (y itself, about
+ * N*Cout*(H-2)*(W-2)*4 bytes, plus statistics) comes from the library's pool
+ * on `stream`.  (LSE_CONV_CHAIN=1 has the convolution's epilogue compute each
+ * tile's group statistics instead, merged before one apply pass over y;
+ * LSE_CONV_CHAIN=2 keeps y out of memory: the convolution runs twice and the
+ * second pass finishes the chain from the tensor-core accumulators.  Both
+ * measured slower on GB300.)
  */
 lse_status_t conv_gn_act_lse(const float* x, const float* w, const float* b, const float* gamma,
                              const float* beta, float* out, int64_t N, int64_t Cin, int64_t H, int64_t W,

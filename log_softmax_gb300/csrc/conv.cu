@@ -424,13 +424,18 @@ __global__ void __launch_bounds__(256) gn_tile_merge_kernel(const float4* __rest
 // with LSE_CONV_CHAIN=2 y never reaches memory -- a one-product pass for the
 // partials, then the convolution again, finishing the chain from tensor memory
 // (HBM: x twice, out; twice the tensor work).
-static bool conv_chain_y_free() { return env_int("LSE_CONV_CHAIN", 1) == 2; }
+// 1: the convolution writes y and its tiles' statistics, then merge and apply;
+// 2: y never in memory (statistics pass, then the convolution again);
+// 3 (default): the convolution writes y, then the GroupNorm work queue over y.
+static int conv_chain_mode() { return env_int("LSE_CONV_CHAIN", 3); }
+static bool conv_chain_y_free() { return conv_chain_mode() == 2; }
 
 size_t conv_chain_scratch_bytes(int64_t N, int64_t H, int64_t W, int64_t cout, int64_t G) {
     const int64_t tiles = ((H - 2) * W + kConvTileM - 1) / kConvTileM;  // wide pixels
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
     const size_t y = conv_chain_y_free() ? 0 : up((size_t)N * cout * (H - 2) * (W - 2) * 4);
-    return y + up((size_t)N * tiles * G * sizeof(float4)) + up((size_t)N * G * 8);
+    return y + std::max(up((size_t)N * tiles * G * sizeof(float4)) + up((size_t)N * G * 8),
+                        up(gn_fused_scratch_bytes(N, G, 0)));
 }
 
 cudaError_t launch_conv_gn_act_lse(const DeviceInfo& dev, const float* x, const float* w, const float* b,
@@ -444,6 +449,13 @@ cudaError_t launch_conv_gn_act_lse(const DeviceInfo& dev, const float* x, const 
     float* y = y_free ? nullptr : reinterpret_cast<float*>(sp);
     if (!y_free) sp += up((size_t)N * cout * ohw * 4);
     ConvArgs a = conv_args(dev, x, w, b, y, N, cin, H, W, cout);
+    if (conv_chain_mode() == 3) {
+        // y, then the one-kernel GroupNorm chain over it, samples last to first so
+        // that its first statistics reads find the convolution's last samples in L2
+        cudaError_t e = conv_go<8, 0, kConvWriteY>(dev, a, stream);
+        if (e != cudaSuccess) return e;
+        return launch_gn_act_lse_fused(dev, y, gamma, beta, out, N, cout, ohw, G, eps, sp, stream, 0, true);
+    }
     a.G = (int)G;
     a.cpg = (int)(cout / G);
     a.partials = reinterpret_cast<float4*>(sp);

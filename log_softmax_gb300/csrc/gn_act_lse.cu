@@ -262,6 +262,7 @@ struct GnFusedArgs {
     unsigned long long* next;  // work-item counter, zero at launch
     unsigned stats_target;     // statistics parts an apply tile waits for (G * parts)
     int* status;
+    int reverse;               // walk the samples last to first
 };
 
 // Work items are claimed from one counter in a fixed order: for k = 0, 1, ...:
@@ -315,6 +316,7 @@ __global__ void __launch_bounds__(T) gn_fused_kernel(const GnFusedArgs a) {
             idx = u - (n - (N - lag)) * TT;
             is_stats = false;
         }
+        if (a.reverse) n = N - 1 - n;
         if (is_stats) {
             const int64_t g = idx / P, p = idx - (idx / P) * P;
             const int64_t nv = (int64_t)cpg * HW / VEC;
@@ -469,7 +471,8 @@ static cudaError_t gn_fused_go(const DeviceInfo& dev, const GnFusedArgs& args, s
 
 cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const float* gamma,
                                     const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
-                                    int64_t G, float eps, void* scratch, cudaStream_t stream, int out_kind) {
+                                    int64_t G, float eps, void* scratch, cudaStream_t stream, int out_kind,
+                                    bool reverse) {
     const bool vec = (HW % 4 == 0) && ((reinterpret_cast<uintptr_t>(y) & 15) == 0) &&
                      ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
     const int VEC = vec ? 4 : 1;
@@ -498,6 +501,7 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     const size_t done_bytes = ((size_t)N * sizeof(unsigned) + 15) / 16 * 16;
     args.next = reinterpret_cast<unsigned long long*>(sp + done_bytes);
     args.status = dev.status;
+    args.reverse = reverse ? 1 : 0;
     cudaError_t e = cudaMemsetAsync(args.done, 0, done_bytes + 16, stream);
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)C * sizeof(float4);

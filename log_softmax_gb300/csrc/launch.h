@@ -88,7 +88,7 @@ size_t gn_fused_scratch_bytes(int64_t N, int64_t G, int out_kind);
 cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const float* gamma,
                                     const float* beta, float* out, int64_t N, int64_t C, int64_t HW,
                                     int64_t G, float eps, void* scratch, cudaStream_t stream,
-                                    int out_kind = 0);
+                                    int out_kind = 0, bool reverse = false);
 
 // Form 3 (and GroupNorm alone, and the chain before its lse) on the same
 // work-queue schedule, each item staged through a ring of shared-memory slots

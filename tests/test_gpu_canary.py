@@ -91,7 +91,7 @@ def test_groupnorm_ops(lib, shift, monkeypatch):
 
 @pytest.mark.parametrize("shift", [0, 1])
 def test_conv_ops(lib, shift, monkeypatch):
-    for chain in ("1", "2"):
+    for chain in ("1", "2", "3"):
         monkeypatch.setenv("LSE_CONV_CHAIN", chain)
         for N, H, W in ((2, 9, 11), (1, 130, 131)):
             inp = synth.make_inputs("conv_gn_act_lse_128x8x128x128", shape=(N, 8, H, W))

@@ -125,7 +125,7 @@ def _chain(L, inp, G, eps=1e-5):
     return out.cpu()
 
 
-@pytest.mark.parametrize("chain", ["1", "2"], ids=["y-round-trip", "y-free"])
+@pytest.mark.parametrize("chain", ["1", "2", "3"], ids=["y-round-trip", "y-free", "y-then-queue"])
 @pytest.mark.parametrize("N,Cin,H,W,Cout,G", CHAIN_CASES)
 def test_conv_chain_parity(lib, N, Cin, H, W, Cout, G, chain, monkeypatch):
     monkeypatch.setenv("LSE_CONV_CHAIN", chain)
@@ -145,7 +145,7 @@ def test_conv2d_nan_input(lib):
     assert_parity(got, oracle.conv2d(inp["x"], inp["w"], inp["bias"]), "conv2d with a NaN input")
 
 
-@pytest.mark.parametrize("chain", ["1", "2"], ids=["y-round-trip", "y-free"])
+@pytest.mark.parametrize("chain", ["1", "2", "3"], ids=["y-round-trip", "y-free", "y-then-queue"])
 def test_conv_chain_nan_input(lib, chain, monkeypatch):
     """A NaN in one sample's input reaches every group mean of that sample, so the
     whole sample's output is NaN; the other sample is untouched."""
