@@ -346,6 +346,30 @@ def pin_gn_act_residual_torch(orc):
     _close(orc.gn_act_residual(y, gamma, beta, G, 1e-5), ref, rtol=1e-12, atol=1e-12)
 
 
+def pin_gn_non_finite(orc):
+    """NaN, +inf or -inf in a group makes that group NaN and leaves the others alone, as
+    float64 torch.nn.functional.group_norm gives; through the channel lse (which spans
+    every group) the whole sample is NaN."""
+    rng = _rng(48)
+    N, C, H, W, G = 4, 8, 3, 3, 4
+    y = rng.normal(0, 1, size=(N, C, H, W)).astype(np.float32)
+    y[0, 2, 1, 1] = np.nan       # sample 0, group 1
+    y[1, 0, 0, 0] = np.inf       # sample 1, group 0
+    y[2, 7, 2, 2] = -np.inf      # sample 2, group 3
+    gamma = rng.uniform(0.5, 1.5, size=C).astype(np.float32)
+    beta = rng.normal(0, 0.3, size=C).astype(np.float32)
+    y64 = torch.from_numpy(y).double()
+    z = F.group_norm(y64, G, torch.from_numpy(gamma).double(), torch.from_numpy(beta).double(),
+                     eps=float(np.float32(1e-5))).numpy()
+    got = np.asarray(orc.group_norm(y, gamma, beta, G, 1e-5), dtype=np.float64).reshape(z.shape)
+    assert np.array_equal(np.isnan(got), np.isnan(z))
+    assert int(np.isnan(got).sum()) == 3 * 2 * 9
+    fin = ~np.isnan(z)
+    _close(got[fin], z[fin], rtol=1e-12, atol=1e-12)
+    lse = np.asarray(orc.gn_act_lse(y, gamma, beta, G, 1e-5), dtype=np.float64).reshape(N, -1)
+    assert np.isnan(lse[:3]).all() and np.isfinite(lse[3]).all()
+
+
 # --------------------------------------------------------------------- Conv2d and the conv-fed chain
 
 def pin_conv_torch(orc):
