@@ -21,3 +21,16 @@ def test_e2e_ceiling_slow_return():
     # the way back is the slow one
     link = {"h2d_gbs": 200.0, "d2h_gbs": 50.0, "both_gbs": 240.0}
     assert bench.e2e_ceiling(2e9, 1e9, 1e9, link) == pytest.approx(2e9 / (1e9 / 50e9) / 1e9)
+
+
+def test_oracle_on_threads():
+    """The all-cores CPU baseline: the oracle on two threads, each on its own share."""
+    import synth
+    w = synth.WORKLOADS["log_softmax_256x4096"]
+    sample = {"x": synth.normal((8, 4096), 2)}
+    b, s, used, done = bench.time_oracle_threads(w, sample, 0.2, 1, 2)
+    assert used == 2 and done >= 2 and b == done * 8 * 4096 and s > 0
+    w = synth.WORKLOADS["gn_act_lse_128x64x126x126"]
+    inp = synth.make_inputs(w, shape=(3, 64, 6, 6))
+    b, s, used, done = bench.time_oracle_threads(w, inp, 0.2, 1, 8)
+    assert used == 3 and done >= 3 and b > 0
