@@ -36,6 +36,15 @@ MUTANTS = [
     ("group_offset", "group_stats(yn + g * cpg * HW,", "group_stats(yn + g * HW,", 0),
     ("channel_lse_drops_max", "return m + log(s);", "return log(s);", 0),
     ("mean_not_subtracted", "double d = (double)p[k] - mean;", "double d = (double)p[k];", 0),
+    ("stats_skip_non_finite",
+     "double sum = 0.0;\n    for (int64_t k = 0; k < count; ++k) sum += (double)p[k];\n"
+     "    double mean = sum / (double)count;\n    double sq = 0.0;\n"
+     "    for (int64_t k = 0; k < count; ++k) {\n        double d = (double)p[k] - mean;",
+     "double sum = 0.0;\n    int64_t nf = 0;\n"
+     "    for (int64_t k = 0; k < count; ++k) if (isfinite(p[k])) { sum += (double)p[k]; ++nf; }\n"
+     "    double mean = nf ? sum / (double)nf : 0.0;\n    double sq = 0.0;\n"
+     "    for (int64_t k = 0; k < count; ++k) {\n        if (!isfinite(p[k])) continue;\n"
+     "        double d = (double)p[k] - mean;", 0),
     ("beta_dropped", " + (double)beta[c];", ";", 0),
     ("softmax_without_exp", "out[r * cols + j] = exp((double)row[j] - lse);",
      "out[r * cols + j] = (double)row[j] - lse;", 0),
