@@ -6,18 +6,23 @@
 // threads each, NS = 1..4 by shared memory); a slot loops over tiles of 128
 // wide pixels (conv_tile.cuh).  The weights are split (hi/lo tf32) into shared
 // memory once per CTA; per tile the slot's threads stage the input window (hi
-// and lo), one thread issues the 27 MMAs into the slot's tensor-memory
-// columns, and after their commit every thread reads its pixel's Cout
-// accumulators back (tcgen05.ld), adds the bias and stores y with coalesced
-// rows per channel.  The slots run independently, so one slot's loads overlap
-// another's MMAs and epilogue.  With CPG > 0 the epilogue also folds each
-// channel group's values of the tile into a Welford (count, mean, M2) -- per
-// thread over the group's channels, then across the tile's pixels through
-// shared memory -- and stores one partial per (sample, tile, group);
-// gn_tile_merge_kernel merges a sample's tiles.  The statistics mode uses one
-// product of round-to-nearest tf32 operands (unbiased errors of ~2^-12
-// relative per product average out over the ~63,000 values of a group: mean
-// and variance stay within ~1e-5 relative), the other modes the 3xTF32 split.
+// and lo), one thread issues the tile's MMAs (18 with the hi and lo weights
+// stacked for Cout <= 64, else 27) into the slot's tensor-memory columns, and
+// after their commit every thread reads its pixel's Cout accumulators back
+// (tcgen05.ld), adds the bias and stores y with coalesced rows per channel.
+// The slots run independently, so one slot's loads overlap another's MMAs and
+// epilogue.  With CPG > 0 the epilogue also takes each channel group's values
+// of the tile to an exact (count, mean, M2) -- per thread over the group's
+// channels, then across the tile's pixels in two passes through shared memory
+// -- and stores one partial per (sample, tile, group); gn_tile_merge_kernel
+// merges a sample's tiles.  The statistics mode uses one product of
+// round-to-nearest tf32 operands (unbiased errors of ~2^-12 relative per
+// product average out over the ~63,000 values of a group: mean and variance
+// stay within ~1e-5 relative), the other modes the 3xTF32 split.
+//
+// conv_gn_act_lse runs, by default, the plain convolution and then the
+// GroupNorm chain's work-queue kernel over y (gn_act_lse.cu); the statistics
+// epilogue above and the form with y never in memory are its alternatives.
 #include <algorithm>
 #include <cstdio>
 

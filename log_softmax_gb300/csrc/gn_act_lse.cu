@@ -16,6 +16,11 @@
 //                    channels, so every load is a coalesced 128-bit read of a
 //                    channel plane; the channel lse is kept online as a
 //                    (max, sum) pair per pixel, one rescale per 8 channels.
+//   gn_fused_kernel  (the default) both in one cooperative kernel: statistics
+//                    parts and apply tiles claimed from one work queue, each
+//                    sample's apply close behind its statistics so that the
+//                    second read of y hits L2 (128-thread CTAs, two parts per
+//                    group for the channel lse).
 #include <algorithm>
 #include <cstdio>
 

@@ -5,11 +5,23 @@
 // kernels give each row one block and read it two or three times from HBM;
 // its traffic analysis judges the ideal of one read plus one write out of
 // reach because a 1.5 MiB row does not fit on one SM.  On GB300 it fits in
-// the shared memory of a thread-block cluster, so the three kernels here are:
+// the shared memory of a group of CTAs, so the kernels here are:
 //
 //  rows_reg_kernel      rows up to 32K floats: the row lives in registers of
 //                       one warp or one block; exact two-pass (max, then sum)
 //                       over registers, one HBM read and one write.
+//  lsm_ws_kernel        (the default for long 16-byte-aligned rows) a row split
+//                       over a group of CTAs of a cooperative grid, each slice
+//                       staged by bulk copies in NB shared-memory buffers;
+//                       fold warps fold each landed chunk and publish the
+//                       CTA's pair through a tagged slot, store warps merge the
+//                       group's pairs, write x - lse from shared memory and
+//                       refill.  One HBM read and one write.
+//  lsm_smem_kernel      the same staging with the pairs merged through a
+//                       cluster's distributed shared memory or in lock step
+//                       (selectable; slower on GB300).
+//  lsm_l2_group_kernel  a group's slices read twice, the second time from L2
+//                       (selectable; slower on GB300).
 //  lsm_smem_cluster     rows up to 16 x ~226 KB: each CTA of a cluster copies
 //                       its slice of the row into shared memory with bulk
 //                       (TMA) copies, folds it into a running (max, sum) pair
