@@ -1,7 +1,7 @@
 """Benchmark of the logsumexp hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline] [--no-configs]
 
 One step is one call of the library on one batch of the workload (default
 log_softmax over the last axis of fp32 x[4096, 393216]: rows a2 + a3 of the
@@ -9,6 +9,11 @@ path, one kernel launch).  Prints one JSON line (rank 0).  Under torchrun each
 rank runs the whole workload on its own GPU (independent batches, weak
 scaling) with no data-path collective; the timed region is bracketed by a
 barrier and a device synchronize, and the slowest rank's time is reported.
+
+On one GPU the line also carries `configs`: every other workload of the path
+(the logsumexp over dim 0 and log_softmax cases, the GroupNorm chain, and the
+operations beside them) measured in the same run after the default one, each
+with its time per call and its fraction of the HBM (or tf32 tensor) peak.
 
 --impl reference times the CPU oracle (a plain double-precision C
 implementation) on a bounded sample of the same workload, on rank 0 only.
@@ -57,13 +62,29 @@ def algorithmic_bytes(w: synth.Workload) -> int:
         C = w.shape[1]
         return 4 * (2 * w.numel + 2 * C)
     if w.op == "conv_gn_act_lse":
-        # x once, y written once by the conv and read once by the GroupNorm pass, out;
-        # weights, bias, gamma, beta
+        # the method's bytes: x once, the weights, bias, gamma and beta, out (the
+        # intermediate y is this design's choice, not the method's; see design_bytes)
         N, Cin, H, W = w.shape
         Cout = w.params["Cout"]
         ohw = (H - 2) * (W - 2)
-        return 4 * (w.numel + 2 * N * Cout * ohw + N * ohw + Cout * (Cin * 9 + 3))
+        return 4 * (w.numel + N * ohw + Cout * (Cin * 9 + 3))
     raise KeyError(w.op)
+
+
+def design_bytes(w: synth.Workload) -> int:
+    """Bytes this design moves per step where it differs from the algorithmic bytes:
+    the conv-fed chain writes y and reads it back once (L2 serves part of the re-read)."""
+    if w.op == "conv_gn_act_lse":
+        N, Cin, H, W = w.shape
+        return algorithmic_bytes(w) + 4 * 2 * N * w.params["Cout"] * (H - 2) * (W - 2)
+    return algorithmic_bytes(w)
+
+
+def conv_flops(w: synth.Workload) -> int:
+    """Multiply-adds of the 3 x 3 convolution counted as 2 flops each (the method's own
+    count; the 3xTF32 split executes three products per multiply-add)."""
+    N, Cin, H, W = w.shape
+    return 2 * N * w.params["Cout"] * (H - 2) * (W - 2) * Cin * 9
 
 
 GN_ELEMENTWISE = ("group_norm", "gn_act_residual")
@@ -143,9 +164,7 @@ def oracle_call(w: synth.Workload, inputs) -> int:
         oracle.conv_gn_act_lse(x, inputs["w"], inputs["bias"], inputs["gamma"], inputs["beta"], w.params["G"],
                                w.params["eps"])
         N, Cin, H, W = x.shape
-        Cout = w.params["Cout"]
-        ohw = (H - 2) * (W - 2)
-        return 4 * (x.numel() + 2 * N * Cout * ohw + N * ohw)
+        return 4 * (x.numel() + N * (H - 2) * (W - 2))
     y, g, b = inputs["y"], inputs["gamma"], inputs["beta"]
     getattr(oracle, w.op)(y, g, b, w.params["G"], w.params["eps"])
     if w.op == "gn_act_lse":
@@ -196,14 +215,48 @@ def rank_seed_offset(rank: int) -> int:
 
 # ------------------------------------------------------------------ peaks, traffic, clocks
 
-def hbm_peak():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _peaks():
     try:
-        with open(p) as f:
-            d = json.load(f)
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except Exception:
+        return None
+
+
+def hbm_peak():
+    d = _peaks()
+    try:
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+# Nominal dense tensor rates of GB300 (PFLOP/s): tf32 1.1 against bf16 2.25.
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def tf32_peak():
+    """The tf32 tensor peak: the measured bf16 burst times the nominal tf32 / bf16 ratio."""
+    d = _peaks()
+    try:
+        return float(d["bf16_tflops"]) * TF32_OVER_BF16, "measured bf16 burst x 1.1/2.25"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS * TF32_OVER_BF16, "fallback 1900 TFLOP/s bf16 x 1.1/2.25"
+
+
+# Special-function (MUFU) results per clock per SM on GB300, measured with a
+# throughput kernel of independent chains: ex2.approx 31.7, rcp.approx 15.9 (the
+# base-2 exponential runs at twice the reciprocal's rate).  The GroupNorm chain's apply
+# step issues per element of y two exponentials (tanh's and the channel lse's) and one
+# reciprocal (tanh's): 2/32 + 1/16 = 1/8 SM clock per element on the special-function unit.
+SFU_EX2_PER_CLK_PER_SM = 32
+SFU_RCP_PER_CLK_PER_SM = 16
+GN_CHAIN_SFU = {"ex2": 2, "rcp": 1}
+
+
+def gn_chain_sfu_clocks_per_element() -> float:
+    return GN_CHAIN_SFU["ex2"] / SFU_EX2_PER_CLK_PER_SM + GN_CHAIN_SFU["rcp"] / SFU_RCP_PER_CLK_PER_SM
 
 
 # The sources that determine each dominant kernel's code (with the shared headers).
@@ -247,44 +300,154 @@ def ncu_traffic(kernel: str, workload: str):
     return None
 
 
+CLOCK_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                     0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def summarize_clocks(samples, windows):
+    """Median SM clock, highest max clock, the throttle reasons seen and the sample
+    count of the samples inside any of `windows` ((t0, t1) wall-clock pairs); all
+    samples when none falls inside.  A sample is (wall time, sm MHz, max MHz, reasons,
+    power W), with None for a field that could not be read."""
+    inside = [p for p in samples if any(t0 <= p[0] <= t1 for (t0, t1) in windows)]
+    window = "timed region"
+    if not inside:
+        inside = list(samples)
+        window = "whole run (no sample fell inside the timed region)"
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                "note": "no clock source available"}
+    sm = [p[1] for p in inside if p[1] is not None]
+    smax = [p[2] for p in inside if p[2] is not None]
+    power = [p[4] for p in inside if p[4] is not None]
+    reasons = sorted({r for p in inside for r in p[3]})
+    out = {"sm_mhz": statistics.median(sm) if sm else None,
+           "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+           "samples": len(inside), "window": window}
+    if sm:
+        out["sm_mhz_min"] = min(sm)
+    if power:
+        out["power_w_max"] = round(max(power), 1)
+    return out
+
+
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (no setting is changed)."""
+    CLOCK_SM = 1
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError("nvmlDeviceGetHandleByUUID failed")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        v = ctypes.c_uint()
+        self.max_mhz = (float(v.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM,
+                                                                            ctypes.byref(v)) == 0 else None)
+        if self.read()[0] is None:
+            raise OSError("nvmlDeviceGetClockInfo failed")
+
+    def read(self):
+        ct = self.ct
+        c, r, pw = ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
+        mhz = float(c.value) if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(c)) == 0 else None
+        reasons = ([n for bit, n in CLOCK_REASON_BITS.items() if r.value & bit]
+                   if self.reasons_fn(self.h, ct.byref(r)) == 0 else [])
+        watts = pw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw)) == 0 else None
+        return mhz, self.max_mhz, reasons, watts
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons, every 100 ms."""
+    """SM clock, throttle reasons and power sampled during the run: in process through
+    NVML every 2 ms (so that even a timed region of a few tens of milliseconds holds
+    samples), else from `nvidia-smi -lms 100`."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
-        self.samples = []  # (wall time, fields)
+    def __init__(self, device_index: int, period: float = 0.002):
+        self.samples = []  # (wall time, sm MHz, max MHz, reasons, power W)
+        self.period = period
         self.proc = None
         self.thread = None
-        uuid = None
+        self.stop_flag = threading.Event()
+        self.active = threading.Event()
+        self.active.set()
+        self.source = None
         try:
-            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.nvml = _Nvml(device_index)
+            self.source = "nvml"
         except Exception:
-            pass
-        self.target = (["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid] if uuid else
-                       ["-i", str(device_index)])
+            self.nvml = None
+        self.device_index = device_index
 
     def start(self):
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.thread.start()
+            return self
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+        except Exception:
+            pass
+        target = (["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid] if uuid else
+                  ["-i", str(self.device_index)])
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", *self.target, f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", *target, f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except Exception:
             self.proc = None
             return self
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread = threading.Thread(target=self._read_smi, daemon=True)
         self.thread.start()
         return self
 
-    def _read(self):
+    def pause(self):
+        """Stops polling (between timed regions) until resume()."""
+        self.active.clear()
+
+    def resume(self):
+        self.active.set()
+
+    def _poll_nvml(self):
+        while not self.stop_flag.is_set():
+            if not self.active.wait(timeout=0.05):
+                continue
+            try:
+                mhz, mx, reasons, watts = self.nvml.read()
+                self.samples.append((time.time(), mhz, mx, reasons, watts))
+            except Exception:
+                return
+            time.sleep(self.period)
+
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
         for line in self.proc.stdout:
-            parts = [p.strip() for p in line.strip().split(",")]
-            if len(parts) >= 8:
-                self.samples.append((time.time(), parts))
+            p = [q.strip() for q in line.strip().split(",")]
+            if len(p) >= 8:
+                reasons = [n for n, v in zip(names, p[4:8]) if v == "Active"]
+                self.samples.append((time.time(), num(p[0]), num(p[1]), reasons, num(p[2])))
 
     def stop(self):
+        self.stop_flag.set()
+        self.active.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -295,27 +458,9 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float):
-        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
-        window = "timed region"
-        if not inside:
-            inside = [p for (_, p) in self.samples]
-            window = "whole run (no sample fell inside the timed region)"
-        if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
-
-        def num(s):
-            try:
-                return float(s)
-            except ValueError:
-                return None
-        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
-        smax = [num(p[1]) for p in inside if num(p[1]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for p in inside for n, v in zip(names, p[4:8]) if v.strip() == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(inside), "window": window}
+        out = summarize_clocks(list(self.samples), [(t0, t1)])
+        out["source"] = self.source
+        return out
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -493,6 +638,164 @@ def run_reference(args, w: synth.Workload):
     return 0
 
 
+def time_steps(step, steps, flush, stream, dev, world=1):
+    """Times `steps` calls of `step` on `stream` with CUDA events, each preceded by an
+    L2 flush (a write of `flush`) when `flush` is given; bracketed by a barrier and a
+    device synchronize.  Returns (per-step ms, whole-region ms, wall t0, wall t1)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    t_all0.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(1.0)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall1 = time.time()
+    return [a.elapsed_time(b) for a, b in ev], t_all0.elapsed_time(t_all1), wall0, wall1
+
+
+def l2_flush_buffer(inputs, dev):
+    """A buffer of twice the L2 size to write between steps when the inputs would fit
+    in L2 (None when they are larger than twice L2 and need no flush)."""
+    in_bytes = sum(t.numel() * 4 for t in inputs.values())
+    if in_bytes < 2 * L2_BYTES:
+        return torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    return None
+
+
+def hbm_roofline(nbytes, launch_ms, dominant, workload, note):
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / (launch_ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dominant, workload),
+            "kernel": dominant, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6800 GB/s",
+            "note": note}
+
+
+# The workloads measured beside the default line, in the same run (SURVEY rows in
+# brackets): the five configurations of the path, then the rows next to it.
+CONFIG_ROLES = (
+    ("lse_dim0_4x10x32", "C1 (a1)", "latency"),
+    ("log_softmax_256x4096", "C2 (a2+a3)", "latency"),
+    ("lse_dim0_32x8192x4096", "C3 (a1)", "hbm"),
+    ("log_softmax_4096x393216", "C4 (a2+a3)", "default"),
+    ("gn_act_lse_128x64x126x126", "C5 (a4+a5)", "hbm"),
+    ("softmax_4096x393216", "NEXT-2", "hbm"),
+    ("group_norm_128x64x126x126", "NEXT-3", "hbm"),
+    ("gn_act_residual_128x64x126x126", "NEXT-3", "hbm"),
+    ("log_softmax_dim0_32x8192x4096", "NEXT-4", "hbm"),
+    ("conv_gn_act_lse_128x8x128x128", "NEXT-1", "tensor"),
+)
+
+
+def measure_config(L, name: str, role: str, kind: str, dev, stream, steps: int, warmup: int, sampler):
+    """One workload of CONFIG_ROLES measured on this GPU: time per call and, for the
+    bandwidth-bound ones, GB/s on algorithmic bytes and the fraction of the HBM peak;
+    latency-bound ones report microseconds per call after an L2 flush and warm."""
+    w = synth.WORKLOADS[name]
+    inputs = synth.make_inputs(w, device=dev)
+    out = torch.empty(out_shape(w), dtype=torch.float32, device=dev)
+    step = make_step(L, w, inputs, out, stream)
+    if sampler is not None:
+        sampler.resume()
+    nbytes = algorithmic_bytes(w)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if kind == "latency" \
+        else l2_flush_buffer(inputs, dev)
+    for _ in range(warmup):
+        if flush is not None:
+            flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    per, region, t0, t1 = time_steps(step, steps, flush, stream, dev)
+    res = {"role": role, "kernels": LAUNCHES[w.op], "steps": steps, "shape": list(w.shape),
+           "algorithmic_bytes": nbytes}
+    windows = [(t0, t1)]
+    if kind == "latency":
+        med = statistics.median(per)
+        res.update({"us_per_call_l2_flushed": round(1e3 * med, 2),
+                    "gbs_l2_flushed": round(nbytes / (med / 1e3) / 1e9, 2)})
+        # warm: the calls captured back to back in one CUDA graph and replayed, so that
+        # neither the host's enqueue time nor an L2 flush sits between them
+        gstep = make_step(L, w, inputs, out, None)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            gstep()  # outside the capture: the library's first-call set-up
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(steps):
+                gstep()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        per_w, _, t0w, t1w = time_steps(graph.replay, 3, None, stream, dev)
+        us_w = 1e3 * min(per_w) / steps
+        res.update({"us_per_call_warm": round(us_w, 3),
+                    "gbs_warm": round(nbytes / (us_w / 1e6) / 1e9, 2),
+                    "note": "flushed: median CUDA-event time of one call after a 258 MB write; warm: "
+                            f"{steps} calls back to back in one CUDA graph, best of 3 replays / {steps}"})
+        windows.append((t0w, t1w))
+        del graph
+    else:
+        ms = statistics.mean(per) if flush is not None else region / steps
+        peak, _ = hbm_peak()
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res.update({"ms_per_step": round(ms, 5), "gbs": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
+                    "l2": "inputs larger than L2; no flush" if flush is None else
+                    "L2 flushed between steps; steps timed alone"})
+        if w.op == "gn_act_lse":
+            res["sfu"] = {"ops_per_element": dict(GN_CHAIN_SFU)}
+        if kind == "tensor":
+            fl = conv_flops(w)
+            tpk, src = tf32_peak()
+            res.update({"tflops_method": round(fl / (ms / 1e3) / 1e12, 2), "tf32_peak_tflops": round(tpk, 1),
+                        "frac_of_tf32_peak": round(fl / (ms / 1e3) / 1e12 / tpk, 4), "tf32_peak_source": src,
+                        "design_bytes": design_bytes(w),
+                        "note": "bytes are the method's (x, parameters, out); the design also writes the "
+                                "conv output y and reads it back (design_bytes)"})
+            # the convolution alone, into a y buffer
+            N, Cin, H, W = w.shape
+            Cout = w.params["Cout"]
+            y = torch.empty((N, Cout, H - 2, W - 2), dtype=torch.float32, device=dev)
+            xc, wc, bc = inputs["x"], inputs["w"], inputs["bias"]
+            conv = lambda: L.conv2d_3x3(xc, wc, bc, y, N, Cin, H, W, Cout, stream=stream)  # noqa: E731
+            for _ in range(warmup):
+                if flush is not None:
+                    flush.fill_(1.0)
+                conv()
+            per_c, _, t0c, t1c = time_steps(conv, steps, flush, stream, dev)
+            ms_c = statistics.mean(per_c)
+            res["conv2d_3x3"] = {"kernel": "conv2d_tc_kernel", "ms_per_call": round(ms_c, 5),
+                                 "tflops_method": round(fl / (ms_c / 1e3) / 1e12, 2),
+                                 "frac_of_tf32_peak": round(fl / (ms_c / 1e3) / 1e12 / tpk, 4)}
+            windows.append((t0c, t1c))
+            del y
+    if sampler is not None:
+        sampler.pause()
+        c = summarize_clocks(list(sampler.samples), windows)
+        res["clocks"] = {k: c.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "window")}
+        if w.op == "gn_act_lse" and c.get("sm_mhz"):
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            floor_s = gn_chain_sfu_clocks_per_element() * w.numel / sms / (c["sm_mhz"] * 1e6)
+            res["sfu"].update({"floor_ms": round(1e3 * floor_s, 5),
+                               "frac": round(floor_s / (res["ms_per_step"] / 1e3), 4),
+                               "note": f"ex2 at {SFU_EX2_PER_CLK_PER_SM} and rcp at {SFU_RCP_PER_CLK_PER_SM} "
+                                       f"results per clock per SM, {sms} SMs, median SM clock of the window"})
+    del inputs, out, flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, w: synth.Workload):
     world, rank, local = dist_env()
     backend = "nccl" if torch.cuda.is_available() else "gloo"
@@ -519,10 +822,9 @@ def run_ours(args, w: synth.Workload):
     stream = torch.cuda.current_stream(dev)
     step = make_step(L, w, inputs, out, stream)
     nbytes = algorithmic_bytes(w)
-    in_bytes = sum(t.numel() * 4 for t in inputs.values())
-    flush = None
-    if in_bytes < 2 * L2_BYTES:
-        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = l2_flush_buffer(inputs, dev)
+    l2_note = ("inputs larger than L2 (129 MB); no flush" if flush is None else
+               "L2 flushed (256 MB write) between steps; steps timed alone")
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -534,32 +836,13 @@ def run_ours(args, w: synth.Workload):
 
     sampler = ClockSampler(local).start() if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    t_all0 = torch.cuda.Event(enable_timing=True)
-    t_all1 = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    wall0 = time.time()
-    t_all0.record(stream)
-    for i in range(args.steps):
-        if flush is not None:
-            flush.fill_(1.0)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    t_all1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    wall1 = time.time()
+    per_step_ms, region_ms, wall0, wall1 = time_steps(step, args.steps, flush, stream, dev, world)
     if sampler:
-        time.sleep(0.15)
-        sampler.stop()
+        time.sleep(0.01)
+        sampler.pause()  # no polling during the end-to-end and CPU measurements
     status = L.lse_device_status()
 
-    per_step_ms = [a.elapsed_time(b) for a, b in ev]
     kernel_ms = sum(per_step_ms)
-    region_ms = t_all0.elapsed_time(t_all1)
     # With inputs larger than L2 nothing runs between steps: time the whole region.
     # Otherwise an L2 flush runs between steps; time the steps alone.
     local_ms = kernel_ms if flush is not None else region_ms
@@ -568,17 +851,19 @@ def run_ours(args, w: synth.Workload):
     value = total_bytes / (slow_ms / 1e3) / 1e9
 
     # roofline of the dominant kernel (one launch of it per step)
-    peak, peak_kind = hbm_peak()
     launch_ms = statistics.mean(per_step_ms)
-    achieved = nbytes / (launch_ms / 1e3) / 1e9
     dominant = LAUNCHES[w.op][0]
     achieved_note = ("one launch per step" if len(LAUNCHES[w.op]) == 1 else
                      f"{len(LAUNCHES[w.op])} launches per step ({', '.join(LAUNCHES[w.op])}); achieved over the whole step")
-    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dominant, w.name),
-                "kernel": dominant, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6800 GB/s",
-                "note": achieved_note}
+    if w.op == "conv_gn_act_lse":
+        tpk, src = tf32_peak()
+        ach = conv_flops(w) / (launch_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(ach, 2), "peak": round(tpk, 1), "unit": "TFLOP/s",
+                    "frac": round(ach / tpk, 4), "traffic": ncu_traffic(dominant, w.name), "kernel": dominant,
+                    "peak_source": src, "note": achieved_note + "; flops are the convolution's multiply-adds x 2",
+                    "hbm": hbm_roofline(nbytes, launch_ms, dominant, w.name, "the method's bytes (x, out)")}
+    else:
+        roofline = hbm_roofline(nbytes, launch_ms, dominant, w.name, achieved_note)
 
     # end to end through the public API: pinned host in -> device -> host out, every step
     e2e = None
@@ -605,6 +890,29 @@ def run_ours(args, w: synth.Workload):
         except Exception as e:  # the single-threaded figure stands alone
             cpu["all_cores"] = {"unavailable": repr(e)[:200]}
 
+    # the other workloads of the path, measured in this same run (one GPU only)
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs and not args.shape:
+        del inputs, out, flush, step
+        torch.cuda.empty_cache()
+        configs = {}
+        for name, role, kind in CONFIG_ROLES:
+            if kind == "default":
+                configs[name] = {"role": role, "see": "this line's value" if name == w.name else
+                                 "python bench.py (default workload)"}
+                if name != w.name:
+                    kind = "hbm"
+                else:
+                    continue
+            try:
+                configs[name] = measure_config(L, name, role, kind, dev, stream, args.config_steps, 3, sampler)
+            except Exception as e:  # one workload's failure does not hide the others
+                configs[name] = {"role": role, "error": repr(e)[:300]}
+        status = status or L.lse_device_status()
+    if sampler:
+        time.sleep(0.05)
+        sampler.stop()
+
     if rank != 0:
         return 0
     clocks = sampler.summary(wall0, wall1) if sampler else None
@@ -617,8 +925,7 @@ def run_ours(args, w: synth.Workload):
         "data": "synthetic",
         "config": {"workload": w.name, "shape": list(w.shape), "recipe": w.recipe,
                    "algorithmic_bytes_per_step": nbytes,
-                   "l2": ("inputs larger than L2 (129 MB); no flush" if flush is None else
-                          "L2 flushed (256 MB write) between steps; steps timed alone"),
+                   "l2": l2_note,
                    "parallelism": f"replicas x{world} (independent batches)"},
         "roofline": roofline,
         "e2e": e2e,
@@ -626,6 +933,7 @@ def run_ours(args, w: synth.Workload):
         "clocks": clocks,
         "gpu_launches": len(LAUNCHES[w.op]) * args.steps,
         "device_status": L.lse_status_string(status),
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -747,6 +1055,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads measured after the default line")
+    ap.add_argument("--config-steps", type=int, default=20)
     ap.add_argument("--shape", default=None,
                     help="comma-separated shape: the workload's recipe at another size "
                          "(smaller cases for profiling; not a bench line)")

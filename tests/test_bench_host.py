@@ -34,3 +34,32 @@ def test_oracle_on_threads():
     inp = synth.make_inputs(w, shape=(3, 64, 6, 6))
     b, s, used, done = bench.time_oracle_threads(w, inp, 0.2, 1, 8)
     assert used == 3 and done >= 3 and b > 0
+
+
+def test_clock_summary_keeps_the_timed_window():
+    # samples every 2 ms; the window holds four of them, one with a power-cap reason
+    samples = [(0.000 + 0.002 * i, 2070.0 - (i == 7) * 300, 2070.0, ["sw_power_cap"] if i == 6 else [], 900.0 + i)
+               for i in range(20)]
+    c = bench.summarize_clocks(samples, [(0.0095, 0.0155)])
+    assert c["samples"] == 3 and c["window"] == "timed region"
+    assert c["sm_mhz"] == 2070.0 and c["sm_mhz_min"] == 1770.0 and c["reasons"] == ["sw_power_cap"]
+    assert c["power_w_max"] == 907.0
+    # two windows are pooled
+    c = bench.summarize_clocks(samples, [(0.0, 0.001), (0.037, 0.039)])
+    assert c["samples"] == 2
+
+
+def test_clock_summary_without_samples_in_the_window():
+    samples = [(1.0, 1900.0, 2070.0, [], None)]
+    c = bench.summarize_clocks(samples, [(5.0, 6.0)])
+    assert c["samples"] == 1 and c["window"].startswith("whole run")
+    assert bench.summarize_clocks([], [(0.0, 1.0)])["samples"] == 0
+
+
+def test_conv_chain_counts_the_method_bytes():
+    import synth
+    w = synth.WORKLOADS["conv_gn_act_lse_128x8x128x128"]
+    # x once, weights + bias + gamma + beta, out [128, 126, 126]
+    assert bench.algorithmic_bytes(w) == 4 * (128 * 8 * 128 * 128 + 64 * (72 + 3) + 128 * 126 * 126)
+    assert bench.design_bytes(w) - bench.algorithmic_bytes(w) == 8 * 128 * 64 * 126 * 126
+    assert bench.conv_flops(w) == 2 * 128 * 64 * 126 * 126 * 72
