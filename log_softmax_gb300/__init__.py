@@ -22,6 +22,9 @@ Conveniences that allocate the output with torch:
     gn_act_lse_forward(y, gamma, beta, G, eps), group_norm_forward(...),
     gn_act_residual_forward(...), conv2d_3x3_forward(x, w, b),
     conv_gn_act_lse_forward(x, w, b, gamma, beta, G, eps)
+Given host (CPU) tensors, a convenience returns a host result after synchronising,
+and raises LseError(LSE_ERR_TIMEOUT) if a bounded wait in a kernel gave up on the
+device; given CUDA tensors it returns at once and lse_device_status() reports.
 """
 from __future__ import annotations
 
@@ -282,15 +285,32 @@ def _to_device(t: torch.Tensor, device):
     return t.contiguous().to(device, non_blocking=True), True
 
 
-def _result(dev_out: torch.Tensor, was_host: bool, out):
+def _raise_on_device_timeout(fn: str, stream) -> None:
+    """After a synchronisation: reads (and clears) the library's device status and
+    raises LseError(LSE_ERR_TIMEOUT) when a bounded wait in a kernel gave up, since
+    that call's outputs are then unspecified.  The status word is per device, so a
+    timeout of another call on the same device that completed meanwhile is
+    reported here too."""
+    rc = load_library().lse_device_status(stream)
+    if rc != 0:
+        raise LseError(fn, rc, "a kernel's bounded wait gave up; the outputs are unspecified"
+                       if rc == 7 else "")
+
+
+def _result(dev_out: torch.Tensor, was_host: bool, out, fn: str = "call"):
     """Returns the device result, or copies it to host memory (`out` if given, else
-    a new pinned tensor) when the input came from the host."""
+    a new pinned tensor) when the input came from the host.  The host path
+    synchronises, so it also checks the device status (see _raise_on_device_timeout);
+    a device result is returned while the call may still run, unchecked."""
     if not was_host:
         return dev_out
     host = out if out is not None else torch.empty(dev_out.shape, dtype=dev_out.dtype,
                                                    pin_memory=True)
+    stream = torch.cuda.current_stream(dev_out.device)
     host.copy_(dev_out.view(host.shape), non_blocking=True)
-    torch.cuda.current_stream(dev_out.device).synchronize()
+    stream.synchronize()
+    with torch.cuda.device(dev_out.device):
+        _raise_on_device_timeout(fn, stream.cuda_stream)
     return host
 
 
@@ -320,7 +340,7 @@ def logsumexp(x: torch.Tensor, dim: int = 0, keepdim: bool = False, out=None,
     out_shape = shape[:dim] + ([1] if keepdim else []) + shape[dim + 1:]
     res = _device_out(out_shape, xd, host, out)
     lse_reduce(xd, res, outer, R, inner)
-    return _result(res, host, out)
+    return _result(res, host, out, "logsumexp")
 
 
 def _split(shape, dim):
@@ -343,7 +363,7 @@ def log_softmax(x: torch.Tensor, out=None, device="cuda", *, dim: int = -1) -> t
         outer, R, inner = _split(list(xd.shape), dim % xd.ndim)
         res = _device_out(xd.shape, xd, host, out)
         log_softmax_dim(xd, res, outer, R, inner)
-        return _result(res, host, out)
+        return _result(res, host, out, "log_softmax")
     if not x.is_cuda:
         # host in, host out: the library pipelines chunks through the device
         xh = x.contiguous()
@@ -355,13 +375,14 @@ def log_softmax(x: torch.Tensor, out=None, device="cuda", *, dim: int = -1) -> t
             stream = torch.cuda.current_stream()
             log_softmax_lastdim_host(xh, oh, rows, cols, stream=stream)
             stream.synchronize()
+            _raise_on_device_timeout("log_softmax", stream.cuda_stream)
         return oh
     xd, host = _to_device(x, device)
     cols = xd.shape[-1] if xd.ndim else 1
     rows = xd.numel() // cols if cols else 0
     res = _device_out(xd.shape, xd, host, out)
     log_softmax_lastdim(xd, res, rows, cols)
-    return _result(res, host, out)
+    return _result(res, host, out, "log_softmax")
 
 
 def softmax(x: torch.Tensor, out=None, device="cuda") -> torch.Tensor:
@@ -371,7 +392,7 @@ def softmax(x: torch.Tensor, out=None, device="cuda") -> torch.Tensor:
     rows = xd.numel() // cols if cols else 0
     res = _device_out(xd.shape, xd, host, out)
     softmax_lastdim(xd, res, rows, cols)
-    return _result(res, host, out)
+    return _result(res, host, out, "softmax")
 
 
 def _gn_call(fn, y, gamma, beta, G, eps, out, device):
@@ -384,7 +405,7 @@ def _gn_call(fn, y, gamma, beta, G, eps, out, device):
         HW *= s
     res = _device_out(yd.shape, yd, host, out)
     fn(yd, gd, bd, res, N, C, HW, G, eps)
-    return _result(res, host, out)
+    return _result(res, host, out, fn.__name__)
 
 
 def group_norm_forward(y: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, G: int,
@@ -409,7 +430,7 @@ def conv2d_3x3_forward(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor, out=No
     Cout = wd.shape[0]
     res = _device_out((N, Cout, H - 2, W - 2), xd, host, out)
     conv2d_3x3(xd, wd, bd, res, N, Cin, H, W, Cout)
-    return _result(res, host, out)
+    return _result(res, host, out, "conv2d_3x3_forward")
 
 
 def conv_gn_act_lse_forward(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor, gamma: torch.Tensor,
@@ -421,7 +442,7 @@ def conv_gn_act_lse_forward(x: torch.Tensor, w: torch.Tensor, b: torch.Tensor, g
     N, Cin, H, W = xd.shape
     res = _device_out((N, 1, H - 2, W - 2), xd, host, out)
     conv_gn_act_lse(xd, wd, bd, gd, betad, res, N, Cin, H, W, wd.shape[0], G, eps)
-    return _result(res, host, out)
+    return _result(res, host, out, "conv_gn_act_lse_forward")
 
 
 def gn_act_lse_forward(y: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, G: int,
@@ -438,4 +459,4 @@ def gn_act_lse_forward(y: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor,
         HW *= s
     res = _device_out([N, 1] + spatial, yd, host, out)
     gn_act_lse(yd, gd, bd, res, N, C, HW, G, eps)
-    return _result(res, host, out)
+    return _result(res, host, out, "gn_act_lse_forward")

@@ -76,3 +76,20 @@ def test_bounded_wait_timeout_is_reported(lib, monkeypatch):
     torch.cuda.synchronize()
     assert lib.lse_device_status() == 0
     assert_parity(out.cpu(), oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], 16, 1e-5), "after")
+
+
+def test_timeout_raises_through_a_convenience(lib, monkeypatch):
+    """A convenience that returns a host result synchronises, so it reads the device
+    status: a bounded wait that ran out becomes LseError(LSE_ERR_TIMEOUT) instead of
+    a silently unspecified result, and the next call works."""
+    inp = _gn_inputs()
+    monkeypatch.setenv("LSE_GN_VARIANT", "2")
+    monkeypatch.setenv("LSE_TEST_UNREACHABLE_WAIT", "1")
+    with pytest.raises(lib.LseError) as e:
+        lib.gn_act_lse_forward(inp["y"].pin_memory(), inp["gamma"], inp["beta"], 16, 1e-5)
+    assert e.value.status == 7
+    assert lib.lse_device_status() == 0                  # the status was read and cleared
+    monkeypatch.delenv("LSE_TEST_UNREACHABLE_WAIT")
+    got = lib.gn_act_lse_forward(inp["y"].pin_memory(), inp["gamma"], inp["beta"], 16, 1e-5)
+    assert not got.is_cuda
+    assert_parity(got, oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], 16, 1e-5), "after the timeout")
