@@ -266,16 +266,23 @@ lse_status_t gn_act_lse(const float* y, const float* gamma, const float* beta, f
                         cudaStream_t stream);
 
 /*
- * gn_act_lse_noalloc — the same computation and arguments as gn_act_lse, for
- * callers that must not allocate device memory: a plugin or engine whose host
- * framework has reserved all device memory and forbids its components to
- * allocate, or a latency-critical path that cannot take an allocation's cost or
- * its out-of-memory failure mid-step.  (The pages have no counterpart: it is a
+ * gn_act_lse_noalloc — gn_act_lse's result and arguments, for callers that must
+ * not allocate device memory: a plugin or engine whose host framework has
+ * reserved all device memory and forbids its components to allocate, or a
+ * latency-critical path that cannot take an allocation's cost or its
+ * out-of-memory failure mid-step.  (The pages have no counterpart: it is a
  * deployment variant of gn_act_lse.)
+ *   - It runs the two-kernel path (a statistics kernel, then the apply kernel:
+ *     what LSE_GN_VARIANT=1 selects for gn_act_lse), which reads y twice from
+ *     HBM where gn_act_lse's default one-kernel work queue serves most of the
+ *     second read from L2: on y[128, 64, 126, 126] about 0.179 ms against
+ *     0.159 ms on GB300.  Results agree with gn_act_lse's within the tolerance
+ *     above, not bit for bit (the statistics are merged in another order).
  *   - Allocates nothing: the 2*N*G floats of statistics live in a fixed array
  *     compiled into the library (512 KiB, N*G <= 65536), which every GPU that
- *     loads the library holds until the process exits.  N*G > 65536 returns
- *     LSE_ERR_SIZE; every other argument rule is gn_act_lse's.
+ *     loads the library holds until the process exits.  gn_act_lse's argument
+ *     rules are checked first (same status codes); then N*G > 65536 returns
+ *     LSE_ERR_SIZE.
  *   - The first call on a device does a one-time set-up on that device (it looks
  *     up the array's device address with cudaGetSymbolAddress); make that first
  *     call before any stream capture.

@@ -80,10 +80,6 @@ lse_status_t noalloc_device(NoAllocDevice** out) {
     return LSE_OK;
 }
 
-bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
-
-bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-
 }  // namespace
 }  // namespace lse
 
@@ -91,17 +87,13 @@ extern "C" lse_status_t gn_act_lse_noalloc(const float* y, const float* gamma, c
                                            float* out, int64_t N, int64_t C, int64_t HW, int64_t G,
                                            float eps, cudaStream_t stream) {
     using namespace lse;
-    if (N < 0 || HW < 0 || C <= 0 || G <= 0 || C % G != 0) return LSE_ERR_SIZE;
-    if (C > kGnMaxChannels) return LSE_ERR_SIZE;
-    int64_t nchw = 0, nhw = 0, ng = 0;
-    if (!mul_ok(N, C, &nchw) || !mul_ok(nchw, HW, &nchw) || nchw > INT64_MAX / 4 ||
-        !mul_ok(N, HW, &nhw) || !mul_ok(N, G, &ng))
-        return LSE_ERR_SIZE;
-    if (ng > kNoAllocMaxGroups) return LSE_ERR_SIZE;  // beyond the fixed scratch
-    if (!(eps >= 0.f) || eps == __builtin_inff()) return LSE_ERR_VALUE;
-    if (nhw == 0) return LSE_OK;
-    if (!y || !gamma || !beta || !out) return LSE_ERR_NULL;
-    if (!aligned4(y) || !aligned4(gamma) || !aligned4(beta) || !aligned4(out)) return LSE_ERR_ALIGN;
+    // gn_act_lse's argument rules, then the limit of the fixed scratch (N and G are
+    // known to be positive and N * G not to overflow once check_gn has passed)
+    bool empty = false;
+    lse_status_t st0 = check_gn(y, gamma, beta, out, N, C, HW, G, eps, &empty);
+    if (st0 != LSE_OK) return st0;
+    if (N * G > kNoAllocMaxGroups) return LSE_ERR_SIZE;
+    if (empty) return LSE_OK;
     NoAllocDevice* s = nullptr;
     lse_status_t st = noalloc_device(&s);
     if (st != LSE_OK) return st;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/lse.h"
+
 namespace lse {
 
 struct DeviceInfo {
@@ -119,6 +121,12 @@ cudaError_t launch_conv_gn_act_lse(const DeviceInfo& dev, const float* x, const 
 
 // Largest C that the apply kernel's shared-memory table holds.
 constexpr int64_t kGnMaxChannels = 8192;
+
+// Host-side argument checks of the GroupNorm entry points (sizes, overflow, eps,
+// NULL, alignment), before any CUDA call; *empty is set when the output has no
+// elements (LSE_OK, nothing to launch).
+lse_status_t check_gn(const float* y, const float* gamma, const float* beta, const float* out, int64_t N,
+                      int64_t C, int64_t HW, int64_t G, float eps, bool* empty);
 
 // Reads an integer tuning knob from the environment (default when unset).
 int env_int(const char* name, int dflt);

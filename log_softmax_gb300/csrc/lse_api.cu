@@ -133,6 +133,30 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
+static bool gn_mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+static bool gn_aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Host-side checks shared by the GroupNorm entry points (declared in launch.h).
+lse_status_t check_gn(const float* y, const float* gamma, const float* beta, const float* out, int64_t N,
+                      int64_t C, int64_t HW, int64_t G, float eps, bool* empty) {
+    *empty = false;
+    if (N < 0 || HW < 0 || C <= 0 || G <= 0 || C % G != 0) return LSE_ERR_SIZE;
+    if (C > kGnMaxChannels) return LSE_ERR_SIZE;
+    int64_t nchw = 0, nhw = 0, ng = 0;
+    if (!gn_mul_ok(N, C, &nchw) || !gn_mul_ok(nchw, HW, &nchw) || nchw > INT64_MAX / 4 ||
+        !gn_mul_ok(N, HW, &nhw) || !gn_mul_ok(N, G, &ng))
+        return LSE_ERR_SIZE;
+    if (!(eps >= 0.f) || eps == __builtin_inff()) return LSE_ERR_VALUE;
+    if (nhw == 0) {
+        *empty = true;
+        return LSE_OK;
+    }
+    if (!y || !gamma || !beta || !out) return LSE_ERR_NULL;
+    if (!gn_aligned4(y) || !gn_aligned4(gamma) || !gn_aligned4(beta) || !gn_aligned4(out)) return LSE_ERR_ALIGN;
+    return LSE_OK;
+}
+
 }  // namespace lse
 
 using namespace lse;
@@ -228,26 +252,6 @@ lse_status_t check_rows(const float* x, const float* out, int64_t rows, int64_t 
     }
     if (!x || !out) return LSE_ERR_NULL;
     if (!aligned4(x) || !aligned4(out)) return LSE_ERR_ALIGN;
-    return LSE_OK;
-}
-
-// Host-side checks shared by the GroupNorm entry points.
-lse_status_t check_gn(const float* y, const float* gamma, const float* beta, const float* out, int64_t N,
-                      int64_t C, int64_t HW, int64_t G, float eps, bool* empty) {
-    *empty = false;
-    if (N < 0 || HW < 0 || C <= 0 || G <= 0 || C % G != 0) return LSE_ERR_SIZE;
-    if (C > kGnMaxChannels) return LSE_ERR_SIZE;
-    int64_t nchw = 0, nhw = 0, ng = 0;
-    if (!mul_ok(N, C, &nchw) || !mul_ok(nchw, HW, &nchw) || nchw > INT64_MAX / 4 ||
-        !mul_ok(N, HW, &nhw) || !mul_ok(N, G, &ng))
-        return LSE_ERR_SIZE;
-    if (!(eps >= 0.f) || eps == __builtin_inff()) return LSE_ERR_VALUE;
-    if (nhw == 0) {
-        *empty = true;
-        return LSE_OK;
-    }
-    if (!y || !gamma || !beta || !out) return LSE_ERR_NULL;
-    if (!aligned4(y) || !aligned4(gamma) || !aligned4(beta) || !aligned4(out)) return LSE_ERR_ALIGN;
     return LSE_OK;
 }
 

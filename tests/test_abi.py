@@ -123,6 +123,23 @@ def test_gn_act_lse_validation(lib, args, want):
     assert lib.gn_act_lse(None, None, None, None, N, C, HW, G, eps, None) == want
     assert lib.group_norm(None, None, None, None, N, C, HW, G, eps, None) == want
     assert lib.gn_act_residual(None, None, None, None, N, C, HW, G, eps, None) == want
+    # the no-allocation entry point checks gn_act_lse's rules first, with the same codes
+    assert lib.gn_act_lse_noalloc(None, None, None, None, N, C, HW, G, eps, None) == want
+
+
+NOALLOC_LIMIT_ERRORS = [
+    ((65537, 1, 1, 1, 1e-5), 2),       # one group more than the fixed scratch holds
+    ((4097, 16, 1, 16, 1e-5), 2),
+    ((65537, 1, 1, 1, -1.0), 6),       # a bad eps is reported first, as gn_act_lse does
+    ((4097, 16, 0, 16, 1e-5), 2),      # no outputs, but past the limit: still rejected
+]
+
+
+@pytest.mark.parametrize("args,want", NOALLOC_LIMIT_ERRORS)
+def test_gn_act_lse_noalloc_limit(lib, args, want):
+    N, C, HW, G, eps = args
+    # aligned stand-in addresses: the call must return before touching any of them
+    assert lib.gn_act_lse_noalloc(16, 16, 16, 16, N, C, HW, G, eps, None) == want
 
 
 CONV_ERRORS = [
