@@ -433,12 +433,17 @@ cudaError_t launch_gn_apply(const DeviceInfo& dev, const float* y, const float* 
 // Statistics parts per group and CTA size of the work queue: the channel lse
 // runs 128-thread CTAs with two parts per group (finer items, measured 1.3 %
 // faster than 256 threads and one part), the elementwise outputs 256 threads
-// and one part.  LSE_GN_PARTS / LSE_GN_THREADS override.
+// and one part.  LSE_GN_PARTS / LSE_GN_THREADS override; a thread count other
+// than the compiled 128, 256, 512 and 1024 falls back to the default 128.
 static int gn_parts(int out_kind) {
     return std::max(1, std::min(16, env_int("LSE_GN_PARTS", out_kind == 0 ? 2 : 1)));
 }
 
-static int gn_threads(int out_kind) { return out_kind == 0 ? env_int("LSE_GN_THREADS", 128) : 256; }
+static int gn_threads(int out_kind) {
+    if (out_kind != 0) return 256;
+    const int t = env_int("LSE_GN_THREADS", 128);
+    return (t == 256 || t == 512 || t == 1024) ? t : 128;
+}
 
 size_t gn_fused_scratch_bytes(int64_t N, int64_t G, int out_kind) {
     return (size_t)N * G * gn_parts(out_kind) * sizeof(float4) + ((size_t)N * sizeof(unsigned) + 15) / 16 * 16 + 16;
@@ -512,10 +517,11 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     const size_t smem = (size_t)C * sizeof(float4);
     if (out_kind == 1) return vec ? gn_fused_go<4, 256, 1>(dev, args, smem, stream) : gn_fused_go<1, 256, 1>(dev, args, smem, stream);
     if (out_kind == 2) return vec ? gn_fused_go<4, 256, 2>(dev, args, smem, stream) : gn_fused_go<1, 256, 2>(dev, args, smem, stream);
+    // T is one of the compiled sizes (gn_threads), so args.tiles matches the kernel launched
     if (T == 1024) return vec ? gn_fused_go<4, 1024>(dev, args, smem, stream) : gn_fused_go<1, 1024>(dev, args, smem, stream);
     if (T == 512) return vec ? gn_fused_go<4, 512>(dev, args, smem, stream) : gn_fused_go<1, 512>(dev, args, smem, stream);
-    if (T == 128) return vec ? gn_fused_go<4, 128>(dev, args, smem, stream) : gn_fused_go<1, 128>(dev, args, smem, stream);
-    return vec ? gn_fused_go<4, 256>(dev, args, smem, stream) : gn_fused_go<1, 256>(dev, args, smem, stream);
+    if (T == 256) return vec ? gn_fused_go<4, 256>(dev, args, smem, stream) : gn_fused_go<1, 256>(dev, args, smem, stream);
+    return vec ? gn_fused_go<4, 128>(dev, args, smem, stream) : gn_fused_go<1, 128>(dev, args, smem, stream);
 }
 
 }  // namespace lse
