@@ -16,11 +16,15 @@
 //                    channels, so every load is a coalesced 128-bit read of a
 //                    channel plane; the channel lse is kept online as a
 //                    (max, sum) pair per pixel, one rescale per 8 channels.
+//                    With 16-byte aligned planes the four pixels are two packed
+//                    f32x2 pairs (apply_lse_pairs in gn_common.cuh).
 //   gn_fused_kernel  (the default) both in one cooperative kernel: statistics
 //                    parts and apply tiles claimed from one work queue, each
 //                    sample's apply close behind its statistics so that the
-//                    second read of y hits L2 (128-thread CTAs, two parts per
-//                    group for the channel lse).
+//                    second read of y hits L2 (256-thread CTAs, one part per
+//                    group, a lag of 12 samples for the channel lse).
+// The sample-slice kernel (gn_slab.cu) reads y once instead, keeping slices of
+// each sample in shared memory; it measured slower and is selectable only.
 #include <algorithm>
 #include <cstdio>
 
@@ -185,7 +189,10 @@ __global__ void __launch_bounds__(128) gn_apply_kernel(const float* __restrict__
                                                        const float* __restrict__ stats,
                                                        float* __restrict__ out, int64_t N, int C,
                                                        int64_t HW, int G, int64_t tiles) {
-    extern __shared__ float4 tab[];  // [C] {mean, rstd*gamma*2log2e, beta*2log2e, 0} of the sample
+    // VEC 4: the pair-form table of the sample, [C] {mean, mean, sc, sc} then [C] {sh, sh};
+    // VEC 1: [C] {mean, sc, sh, 0}; sc = rstd*gamma*2log2e, sh = beta*2log2e
+    extern __shared__ float4 tab[];
+    float2* const tab_b = reinterpret_cast<float2*>(tab + C);
     constexpr int T = 128;
     const int tid = threadIdx.x;
     const int cpg = C / G;
@@ -202,14 +209,21 @@ __global__ void __launch_bounds__(128) gn_apply_kernel(const float* __restrict__
                 const int g = c / cpg;
                 const float mean = stats[2 * (n * G + g)];
                 const float rstd = stats[2 * (n * G + g) + 1];
-                tab[c] = make_float4(mean, rstd * gamma[c] * (2.f * kLog2e), beta[c] * (2.f * kLog2e), 0.f);
+                const float sc = rstd * gamma[c] * (2.f * kLog2e), sh = beta[c] * (2.f * kLog2e);
+                if constexpr (VEC == 4)
+                    gn_pair_entry(mean, sc, sh, tab, tab_b, c);
+                else
+                    tab[c] = make_float4(mean, sc, sh, 0.f);
             }
             __syncthreads();
             cur_n = n;
         }
         const int64_t p0 = (tile * T + tid) * VEC;
         if (p0 >= HW) continue;
-        apply_pixels<VEC>(y + n * (int64_t)C * HW + p0, tab, C, HW, out + n * HW + p0);
+        if constexpr (VEC == 4)
+            apply_lse_pairs<false>(y + n * (int64_t)C * HW + p0, tab, tab_b, C, HW, out + n * HW + p0, 0);
+        else
+            apply_pixels<VEC>(y + n * (int64_t)C * HW + p0, tab, C, HW, out + n * HW + p0);
     }
 }
 
@@ -283,7 +297,11 @@ struct GnFusedArgs {
 // (both N x C x HW).
 template <int VEC, int T, int OUT>
 __global__ void __launch_bounds__(T) gn_fused_kernel(const GnFusedArgs a) {
-    extern __shared__ float4 tab[];  // [C] {mean, rstd*gamma*2log2e, beta*2log2e, 0}
+    // The channel lse with VEC 4 takes the pair-form table, [C] {mean, mean, sc, sc} then
+    // [C] {sh, sh}; the other outputs [C] {mean, sc, sh, 0} (see write_pixels).
+    constexpr bool PAIRS = (OUT == 0 && VEC == 4);
+    extern __shared__ float4 tab[];
+    float2* const tab_b = reinterpret_cast<float2*>(tab + a.C);
     __shared__ Welford red[32];
     __shared__ long long item_sh;
     const int tid = threadIdx.x;
@@ -364,14 +382,19 @@ __global__ void __launch_bounds__(T) gn_fused_kernel(const GnFusedArgs a) {
                     acc = wf_merge(acc, Welford{q.x, q.y, q.z});
                 }
                 const float rstd = 1.f / sqrtf(acc.m2 / acc.n + a.eps);
-                const float sc = OUT == 1 ? 1.f : 2.f * kLog2e;
-                tab[c] = make_float4(acc.mean, rstd * a.gamma[c] * sc, a.beta[c] * sc, 0.f);
+                const float k = OUT == 1 ? 1.f : 2.f * kLog2e;
+                if constexpr (PAIRS)
+                    gn_pair_entry(acc.mean, rstd * a.gamma[c] * k, a.beta[c] * k, tab, tab_b, c);
+                else
+                    tab[c] = make_float4(acc.mean, rstd * a.gamma[c] * k, a.beta[c] * k, 0.f);
             }
             __syncthreads();
             const int64_t p0 = (idx * T + tid) * VEC;
             if (p0 < HW) {
                 const float* yp = a.y + n * (int64_t)C * HW + p0;
-                if constexpr (OUT == 0)
+                if constexpr (PAIRS)
+                    apply_lse_pairs<true>(yp, tab, tab_b, C, HW, a.out + n * HW + p0, drop);
+                else if constexpr (OUT == 0)
                     apply_pixels<VEC, true>(yp, tab, C, HW, a.out + n * HW + p0, drop);
                 else
                     write_pixels<VEC, OUT>(yp, tab, C, HW, a.out + n * (int64_t)C * HW + p0, drop);
@@ -409,7 +432,7 @@ cudaError_t launch_gn_apply(const DeviceInfo& dev, const float* y, const float* 
         const int64_t nblk = N * tiles;
         const int64_t cap = (int64_t)dev.sm_count * 16 * 16;
         const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(nblk, cap));
-        const size_t smem = (size_t)C * sizeof(float4);
+        const size_t smem = (size_t)C * (vec_apply ? sizeof(float4) + sizeof(float2) : sizeof(float4));
         cudaError_t e;
         if (vec_apply) {
             if (smem > 48 * 1024) {
@@ -430,19 +453,20 @@ cudaError_t launch_gn_apply(const DeviceInfo& dev, const float* y, const float* 
     }
 }
 
-// Statistics parts per group and CTA size of the work queue: the channel lse
-// runs 128-thread CTAs with two parts per group (finer items, measured 1.3 %
-// faster than 256 threads and one part), the elementwise outputs 256 threads
-// and one part.  LSE_GN_PARTS / LSE_GN_THREADS override; a thread count other
-// than the compiled 128, 256, 512 and 1024 falls back to the default 128.
+// Statistics parts per group and CTA size of the work queue: 256-thread CTAs and
+// one part per group (with the packed-pair apply, measured 3 % faster than 128
+// threads and two parts for the channel lse; the lag of 12 samples 1 % faster than
+// 16).  LSE_GN_PARTS / LSE_GN_THREADS / LSE_GN_LAG override; a thread count other
+// than the compiled 128, 256, 512 and 1024 falls back to the default 256.
 static int gn_parts(int out_kind) {
-    return std::max(1, std::min(16, env_int("LSE_GN_PARTS", out_kind == 0 ? 2 : 1)));
+    (void)out_kind;
+    return std::max(1, std::min(16, env_int("LSE_GN_PARTS", 1)));
 }
 
 static int gn_threads(int out_kind) {
     if (out_kind != 0) return 256;
-    const int t = env_int("LSE_GN_THREADS", 128);
-    return (t == 256 || t == 512 || t == 1024) ? t : 128;
+    const int t = env_int("LSE_GN_THREADS", 256);
+    return (t == 128 || t == 512 || t == 1024) ? t : 256;
 }
 
 size_t gn_fused_scratch_bytes(int64_t N, int64_t G, int out_kind) {
@@ -502,7 +526,7 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     args.stats_target = (unsigned)(G * args.parts) + (env_int("LSE_TEST_UNREACHABLE_WAIT", 0) == 1 ? 1u : 0u);
     const int T = gn_threads(out_kind);
     args.tiles = (int)((HW + (int64_t)T * VEC - 1) / ((int64_t)T * VEC));
-    args.lag = (int)std::min<int64_t>(N, std::max(0, env_int("LSE_GN_LAG", 16)));
+    args.lag = (int)std::min<int64_t>(N, std::max(0, env_int("LSE_GN_LAG", out_kind == 0 ? 12 : 16)));
     args.eps = eps;
     char* sp = static_cast<char*>(scratch);
     args.partials = reinterpret_cast<float4*>(sp);
@@ -514,14 +538,15 @@ cudaError_t launch_gn_act_lse_fused(const DeviceInfo& dev, const float* y, const
     args.reverse = reverse ? 1 : 0;
     cudaError_t e = cudaMemsetAsync(args.done, 0, done_bytes + 16, stream);
     if (e != cudaSuccess) return e;
-    const size_t smem = (size_t)C * sizeof(float4);
+    // the pair-form table of the channel lse takes 24 bytes per channel, the others 16
+    const size_t smem = (size_t)C * ((out_kind == 0 && vec) ? sizeof(float4) + sizeof(float2) : sizeof(float4));
     if (out_kind == 1) return vec ? gn_fused_go<4, 256, 1>(dev, args, smem, stream) : gn_fused_go<1, 256, 1>(dev, args, smem, stream);
     if (out_kind == 2) return vec ? gn_fused_go<4, 256, 2>(dev, args, smem, stream) : gn_fused_go<1, 256, 2>(dev, args, smem, stream);
     // T is one of the compiled sizes (gn_threads), so args.tiles matches the kernel launched
     if (T == 1024) return vec ? gn_fused_go<4, 1024>(dev, args, smem, stream) : gn_fused_go<1, 1024>(dev, args, smem, stream);
     if (T == 512) return vec ? gn_fused_go<4, 512>(dev, args, smem, stream) : gn_fused_go<1, 512>(dev, args, smem, stream);
-    if (T == 256) return vec ? gn_fused_go<4, 256>(dev, args, smem, stream) : gn_fused_go<1, 256>(dev, args, smem, stream);
-    return vec ? gn_fused_go<4, 128>(dev, args, smem, stream) : gn_fused_go<1, 128>(dev, args, smem, stream);
+    if (T == 128) return vec ? gn_fused_go<4, 128>(dev, args, smem, stream) : gn_fused_go<1, 128>(dev, args, smem, stream);
+    return vec ? gn_fused_go<4, 256>(dev, args, smem, stream) : gn_fused_go<1, 256>(dev, args, smem, stream);
 }
 
 }  // namespace lse

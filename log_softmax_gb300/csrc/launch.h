@@ -102,6 +102,21 @@ cudaError_t launch_gn_tma(const DeviceInfo& dev, const float* y, const float* ga
                           int64_t N, int64_t C, int64_t HW, int64_t G, float eps, void* scratch, cudaStream_t stream,
                           int out_kind);
 
+// Form 3 with y read once: each sample split by pixels over a group of CTAs that
+// keep their slices in shared memory and exchange per-group partial statistics
+// through global slots (the channel lse only).  gn_slab_plan says whether it
+// applies (HW % 4 == 0, 16-byte aligned y and out, C <= 256, G <= 64, a slice of
+// two buffers fits) and sizes the launch and its scratch.
+struct GnSlabPlan {
+    int GS = 0, P = 0, NB = 0, groups = 0;
+    size_t smem = 0, scratch_bytes = 0;
+};
+bool gn_slab_plan(const DeviceInfo& dev, const float* y, const float* out, int64_t N, int64_t C, int64_t HW,
+                  int64_t G, GnSlabPlan* plan);
+cudaError_t launch_gn_slab(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
+                           int64_t N, int64_t C, int64_t HW, int64_t G, float eps, const GnSlabPlan& plan,
+                           void* scratch, cudaStream_t stream);
+
 // Conv2d 3 x 3, stride 1, valid, with bias, on the tensor cores (3xTF32):
 // x [N, cin, H, W] -> y [N, cout, H - 2, W - 2].  Shapes conv_tc_supported()
 // accepts: 1 <= cin <= 8, cout a multiple of 16 up to 128, W <= 1024.

@@ -257,10 +257,11 @@ lse_status_t check_rows(const float* x, const float* out, int64_t rows, int64_t 
 
 // The one-kernel GroupNorm chain with output kind out_kind (0 channel lse,
 // 1 GroupNorm, 2 chain before the lse), scratch from the device pool.
-// LSE_GN_VARIANT 2 forces the work-queue kernel with per-thread loads, 3 the
-// one with bulk-copy staging (where it applies); by default the elementwise
-// outputs take the bulk-copy kernel and the channel lse the per-thread one
-// (its apply tiles are bound by arithmetic, not by load latency).
+// By default the channel lse takes the work queue with per-thread loads and the
+// elementwise outputs the bulk-copy work queue.  LSE_GN_VARIANT 2 forces the
+// work-queue kernel with per-thread loads, 3 the one with bulk-copy staging, 4 the
+// sample-slice kernel (y read once, slices kept in shared memory; the channel lse
+// only, where it applies; measured slower on GB300).
 lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, float* out, int64_t N, int64_t C,
                       int64_t HW, int64_t G, float eps, int out_kind, cudaStream_t stream) {
     DeviceState* s = nullptr;
@@ -269,6 +270,20 @@ lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, flo
     cudaMemPool_t pool = nullptr;
     if ((st = device_pool(s, &pool)) != LSE_OK) return st;
     const int variant = env_int("LSE_GN_VARIANT", 0);
+    if (out_kind == 0 && variant == 4) {
+        // the channel lse with y read once: sample slices held in shared memory
+        GnSlabPlan plan;
+        if (gn_slab_plan(s->info, y, out, N, C, HW, G, &plan)) {
+            void* scratch = nullptr;
+            cudaError_t e = pool_alloc(&scratch, plan.scratch_bytes, pool, stream);
+            if (e != cudaSuccess) return cuda_fail(e);
+            e = launch_gn_slab(s->info, y, gamma, beta, out, N, C, HW, G, eps, plan, scratch, stream);
+            cudaError_t ef = cudaFreeAsync(scratch, stream);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (ef != cudaSuccess) return cuda_fail(ef);
+            return LSE_OK;
+        }
+    }
     const bool want_tma = variant == 3 || (variant != 2 && out_kind != 0);
     const bool tma = want_tma && gn_tma_applies(s->info, y, out, C, HW);
     void* scratch = nullptr;

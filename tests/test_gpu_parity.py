@@ -288,6 +288,9 @@ GN_CONFIGS = [
     {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "2", "LSE_GNT_LAG": "2", "LSE_GNT_CTAS_PER_SM": "1"},
     {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "6", "LSE_GNT_LAG": "100"},
     {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "8", "LSE_GNT_CTAS_PER_SM": "1"},
+    {"LSE_GN_VARIANT": "4"},                                    # sample slices in shared memory
+    {"LSE_GN_VARIANT": "4", "LSE_SLAB_NB": "2"},
+    {"LSE_GN_VARIANT": "4", "LSE_SLAB_GROUP": "2"},
 ]
 
 
@@ -314,7 +317,7 @@ def _non_finite_gn_input():
     return y, inp["gamma"], inp["beta"]
 
 
-@pytest.mark.parametrize("variant", ["0", "1", "2", "3"])
+@pytest.mark.parametrize("variant", ["0", "1", "2", "3", "4"])
 def test_gn_act_lse_non_finite(lib, env, variant):
     """A non-finite value makes its group's mean or variance NaN, so every channel of that
     group is NaN at every pixel and the sample's channel lse is NaN everywhere; the
@@ -355,6 +358,32 @@ def test_gn_act_lse_wide_range(lib):
     beta = synth.normal((C,), seed=79, var=4.0)
     got = lib.gn_act_lse_forward(y.to(DEV), gamma.to(DEV), beta.to(DEV), G, 1e-3)
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-3), "gn wide")
+
+
+def test_gn_act_lse_large_mean_small_spread(lib):
+    """Groups whose mean (1e3) is 1e4 times their spread (std 0.1, so rstd ~ 10): z stays
+    accurate (the mean is subtracted before scaling), and the channel lse near 1e3 keeps
+    within the relative part of the tolerance despite the rounding of the exponent's
+    shift (m log2 e).  (Beyond a ratio of ~1e5 no fp32 GroupNorm is accurate: the mean
+    itself is only known to half an ulp, e.g. 5e-4 at 1e4.)"""
+    N, C, H, W, G = 2, 16, 12, 12, 4
+    y = synth.normal((N, C, H, W), seed=81, mean=1.0e3, var=1.0e-2)
+    gamma = synth.uniform((C,), seed=82, lo=0.5, hi=1.5)
+    beta = synth.normal((C,), seed=83, var=0.1)
+    got = lib.gn_act_lse_forward(y.to(DEV), gamma.to(DEV), beta.to(DEV), G, 1e-5)
+    assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-5), "gn mean 1e3, std 0.1")
+
+
+@pytest.mark.parametrize("scale", [1.0e3, 1.0e6, 1.0e15])
+def test_gn_act_lse_large_values(lib, scale):
+    """y of magnitude up to 1e15 with channels far apart: the running max and its
+    rescale carry the channel lse (terms span many binades)."""
+    N, C, H, W, G = 2, 24, 8, 8, 6
+    y = synth.normal((N, C, H, W), seed=84) * scale
+    gamma = synth.uniform((C,), seed=85, lo=0.5, hi=1.5)
+    beta = synth.normal((C,), seed=86, var=0.1)
+    got = lib.gn_act_lse_forward(y.to(DEV), gamma.to(DEV), beta.to(DEV), G, 1e-5)
+    assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-5), f"gn scale {scale}")
 
 
 def test_gn_act_lse_constant_group(lib):
