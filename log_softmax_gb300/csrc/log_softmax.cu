@@ -210,6 +210,7 @@ struct SmemRowArgs {
     int group_size;            // CTAs per row; CTA b is rank b % group_size of group b / group_size
     unsigned long long* slots; // [groups][2][group_size] tagged pairs, all bytes 0xFF at launch
     int softmax;               // warp-specialised kernel: write exp(x - lse) instead of x - lse
+    int ring;                  // ring kernel: chunk slots of shared memory per CTA
 };
 
 // Polls a tagged slot until its tag is `tag`, at most ~1 s / 2^26 polls; on
@@ -619,6 +620,152 @@ __global__ void __launch_bounds__(32 * (FW + SW), 1) lsm_ws_kernel(const SmemRow
     }
 }
 
+// Ring form of the warp-specialised group kernel: a CTA's shared memory is a ring of
+// R chunk slots instead of NB whole-slice buffers, so that the rows in flight need not
+// be a whole number.  Eight groups of 19 CTAs cover all 152 SMs with 81 KB slices, of
+// which 3 would not fit in shared memory; a ring of 8 slots of 27 KB keeps 2.67 rows
+// (216 KB) in flight instead.  Chunk c of the CTA's step j is its chunk
+// g = j * nch + c, held in slot g % R (phase (g / R) & 1); the store warps refill a
+// slot with chunk g + R as soon as they have written chunk g out.  The fold and store
+// roles and the tagged pair slots are those of lsm_ws_kernel: a fold warp publishing
+// row r implies every store warp of the group has read the pairs of row
+// r - 2 ceil(R / nch), so ceil(R / nch) <= kWsSlots / 2 for every CTA of the group
+// (the last, with the shortest slice and fewest chunks, runs furthest ahead) keeps
+// the 16 slots safe.
+constexpr int kRingMax = 64;
+
+template <int FW, int SW>
+__global__ void __launch_bounds__(32 * (FW + SW), 1) lsm_ring_kernel(const SmemRowArgs a) {
+    constexpr int NF = 32 * FW, NS = 32 * SW;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int chunk = a.chunk, R = a.ring;
+    const int64_t rows = a.rows, cols = a.cols;
+    float* const ring = reinterpret_cast<float*>(smem_raw);                                 // [R][chunk]
+    uint64_t* const full = reinterpret_cast<uint64_t*>(smem_raw + (size_t)R * chunk * 4);  // [R]
+    float* const lse_s = reinterpret_cast<float*>(full + kRingMax);                        // [1]
+    MS* const red = reinterpret_cast<MS*>(lse_s + 4);                                      // [2][32]
+
+    const uint32_t GS = (uint32_t)a.group_size;
+    const uint32_t rank = blockIdx.x % GS;
+    const int64_t first_row = blockIdx.x / GS;
+    const int64_t row_step = gridDim.x / GS;
+    unsigned long long* const slots = a.slots + first_row * kWsSlots * GS;  // [kWsSlots][GS]
+    const int64_t c_begin = (int64_t)rank * a.slice;
+    const int len = (int)std::max<int64_t>(0, std::min<int64_t>(a.slice, cols - c_begin));
+    const int nch = (len + chunk - 1) / chunk;
+    const int64_t nrows = first_row < rows ? (rows - first_row + row_step - 1) / row_step : 0;
+    const int64_t total = nrows * nch;  // chunks this CTA moves
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    bool aborted = false;
+
+    if (tid == 0) {
+        for (int r = 0; r < R; ++r) mbar_init(&full[r], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Issuer: the first store thread.  Copies the CTA's chunk g into slot g % R.
+    int64_t issued = 0;
+    auto issue = [&](int64_t g) {
+        if (g >= total || aborted) return;
+        const int64_t j = g / nch;
+        const int c = (int)(g - j * nch);
+        const int sl = (int)(g % R);
+        const int cb = c * chunk;
+        const uint32_t bytes = (uint32_t)std::min(chunk, len - cb) * 4u;
+        fence_proxy_async_smem();  // earlier generic reads of the slot come first
+        mbar_arrive_expect_tx(&full[sl], bytes);
+        bulk_g2s(ring + (size_t)sl * chunk, a.x + (first_row + j * row_step) * cols + c_begin + cb, bytes, &full[sl]);
+        issued = g + 1;
+    };
+    if (tid == NF)
+        for (int g = 0; g < R; ++g) issue(g);
+
+    if (warp < FW) {
+        // ---------------- fold warps: fold, reduce, publish; never wait for the group
+        for (int64_t j = 0; j < nrows; ++j) {
+            MS st = ms_empty();
+            for (int c = 0; c < nch; ++c) {
+                const int64_t g = j * nch + c;
+                const int sl = (int)(g % R);
+                mbar_wait_bounded(&full[sl], (uint32_t)((g / R) & 1), aborted, a.status);
+                const int n4 = std::min(chunk, len - c * chunk) >> 2;
+                const float4* p = reinterpret_cast<const float4*>(ring + (size_t)sl * chunk);
+                int i = tid;
+                for (; i + 3 * NF < n4; i += 4 * NF) {
+                    float v[16];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float4 q = p[i + k * NF];
+                        v[4 * k + 0] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
+                    }
+                    ms_fold<16>(st, v);
+                }
+                for (; i < n4; i += NF) {
+                    float4 q = p[i];
+                    float v[4] = {q.x, q.y, q.z, q.w};
+                    ms_fold<4>(st, v);
+                }
+            }
+            st = ms_warp_allreduce(st);
+            if (lane == 0) red[(j & 1) * 32 + warp] = st;
+            named_bar_sync(1, NF);  // every fold warp is done with this row and its red slot
+            if (warp == 0) {
+                MS r = (lane < FW) ? red[(j & 1) * 32 + lane] : ms_empty();
+                r = ms_warp_allreduce(r);
+                if (lane == 0)
+                    st_relaxed_gpu_u64(slots + (j % kWsSlots) * GS + rank,
+                                       ms_pack_tagged(r, (uint32_t)(j / kWsSlots) & 1u));
+            }
+        }
+    } else {
+        // ---------------- store warps: merge the group's pairs, write, refill
+        const int sid = tid - NF;
+        for (int64_t j = 0; j < nrows; ++j) {
+            if (sid < 32) {
+                MS mine = ms_empty();
+                for (uint32_t k = (uint32_t)sid; k < GS; k += 32) {
+                    const unsigned long long* p = slots + (j % kWsSlots) * GS + k;
+                    const MS other = ms_unpack(poll_slot(p, (uint32_t)(j / kWsSlots) & 1u,
+                                                         ld_relaxed_gpu_u64(p), aborted, a.status));
+                    mine = ms_merge(mine, other);
+                }
+                const float l = ms_lse(ms_warp_allreduce(mine));
+                if (sid == 0) *lse_s = l;
+            }
+            named_bar_sync(2, NS);  // lse_s holds row j's lse
+            const float lse = *lse_s;
+            float* dst = a.out + (first_row + j * row_step) * cols + c_begin;
+            for (int c = 0; c < nch; ++c) {
+                const int64_t g = j * nch + c;
+                const int cb = c * chunk;
+                const int n4 = std::min(chunk, len - cb) >> 2;
+                const float4* p = reinterpret_cast<const float4*>(ring + (size_t)(g % R) * chunk);
+                if (a.softmax) {
+                    for (int i = sid; i < n4; i += NS) st_stream_f4(dst + cb + 4 * i, row_out4(p[i], lse, true));
+                } else {
+                    for (int i = sid; i < n4; i += NS) st_stream_f4(dst + cb + 4 * i, row_out4(p[i], lse, false));
+                }
+                named_bar_sync(2, NS);  // every store warp is done reading chunk g (and lse_s)
+                if (sid == 0) issue(g + R);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == NF && atomicAdd(a.status, 0) != 0) {
+        // After a timeout anywhere, give each slot's last issued fill one more bounded
+        // wait before the shared memory is released.
+        bool again = false;
+        for (int64_t g = std::max<int64_t>(0, issued - R); g < issued; ++g)
+            mbar_wait_bounded(&full[g % R], (uint32_t)((g / R) & 1), again, a.status);
+    }
+}
+
+__host__ inline size_t smem_ring_bytes(int chunk, int ring) {
+    return (size_t)ring * chunk * 4 + (size_t)kRingMax * 8 + 16 + 64 * sizeof(MS);
+}
+
 __host__ inline size_t smem_ws_bytes(int slice, int nb) {
     return (size_t)nb * slice * 4 + (size_t)nb * kSmemMaxChunks * 8 + 16 + 64 * sizeof(MS);
 }
@@ -1005,6 +1152,92 @@ cudaError_t launch_lsm_ws_group(const DeviceInfo& dev, const float* x, float* ou
         case 5: return ws_go_nb<5>(fw, sw, args, p, stream);
         default: return ws_go_nb<3>(fw, sw, args, p, stream);
     }
+}
+
+// ---- ring form of the warp-specialised group kernel
+
+// Group size GS (LSE_WS_GROUP forces it), chunk floats (LSE_RING_CHUNK: the
+// smallest chunk count per slice with chunks of at most that many floats, default
+// 6912 = 27 KB), as many ring slots as fit (at most kRingMax), and at least two
+// slices' worth of slots.  The plan covering the most SM slots wins, then the one
+// with the most rows in flight.  On the 4096 x 393,216 workload (GS = 19, three
+// chunks per slice, 8 slots: 2.67 rows in flight on all 152 SMs) it measured 0.934
+// of the copy peak against 0.950 for lsm_ws_kernel's 144 SMs with 3 rows in flight
+// on the same GPU; 10 KB chunks 0.60, 40 KB chunks 0.90.
+cudaError_t plan_lsm_ring_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
+                                int64_t cols, GroupPlan* plan) {
+    if (cols % 4 != 0 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+        return cudaErrorNotSupported;
+    const int forced = env_int("LSE_WS_GROUP", 0);
+    const int chunk_max = std::max(256, env_int("LSE_RING_CHUNK", 6912) & ~31);
+    double best = -1.0;
+    for (int GS = 1; GS <= kWsMaxGroup; ++GS) {
+        if (forced && GS != forced) continue;
+        const int64_t sl = ((cols + GS - 1) / GS + 31) / 32 * 32;
+        if (sl * (GS - 1) >= cols || sl > (1 << 24)) continue;
+        const int nch = (int)((sl + chunk_max - 1) / chunk_max);
+        const int chunk = (int)(((sl + nch - 1) / nch + 31) / 32 * 32);
+        // the group's last CTA owns the shortest slice, so the fewest chunks per row:
+        // it runs furthest ahead, and bounds the ring (see lsm_ring_kernel)
+        const int64_t last_len = cols - sl * (GS - 1);
+        const int nch_min = (int)std::max<int64_t>(1, (last_len + chunk - 1) / chunk);
+        int R = (int)std::min<int64_t>(kRingMax, ((int64_t)dev.max_smem_optin - (int64_t)smem_ring_bytes(0, 0)) /
+                                                     ((int64_t)chunk * 4));
+        R = std::min(R, (kWsSlots / 2) * nch_min);
+        if (R < 2 * nch) continue;
+        int per_sm = 0;
+        auto kern = lsm_ring_kernel<8, 4>;
+        const size_t smem = smem_ring_bytes(chunk, R);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * 12, smem);
+        if (e != cudaSuccess) return e;
+        const int64_t slots = (int64_t)per_sm * dev.sm_count;
+        const int64_t groups = std::min<int64_t>(rows, slots / GS);
+        if (groups < 1) continue;
+        const double score = (double)(groups * GS) / (double)slots + 0.01 * std::min(3.0, (double)R / nch) -
+                             0.002 * GS;
+        if (score > best) {
+            best = score;
+            plan->threads = 32 * 12;
+            plan->nbuf = R;
+            plan->group_size = GS;
+            plan->groups = (int)groups;
+            plan->slice = (int)sl;
+            plan->chunk = chunk;
+            plan->smem = smem;
+            plan->scratch_bytes = (size_t)groups * kWsSlots * GS * sizeof(unsigned long long);
+        }
+    }
+    return best < 0 ? cudaErrorNotSupported : cudaSuccess;
+}
+
+cudaError_t launch_lsm_ring_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows, int64_t cols,
+                                  const GroupPlan& p, void* scratch, cudaStream_t stream, bool softmax) {
+    (void)dev;
+    cudaError_t e = cudaMemsetAsync(scratch, 0xFF, p.scratch_bytes, stream);
+    if (e != cudaSuccess) return e;
+    if (env_int("LSE_VERBOSE", 0))
+        fprintf(stderr, "[lse] lsm_ring group: GS=%d groups=%d ring=%d slice=%d chunk=%d smem=%zu\n", p.group_size,
+                p.groups, p.nbuf, p.slice, p.chunk, p.smem);
+    SmemRowArgs args{x, out, rows, cols, p.slice, p.chunk, dev.status, p.group_size,
+                     static_cast<unsigned long long*>(scratch), softmax ? 1 : 0, p.nbuf};
+    auto kern = lsm_ring_kernel<8, 4>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the group waits end
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(32 * 12);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cfg.gridDim = dim3((unsigned)(p.groups * p.group_size));
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ rows re-read from L2 by a group

@@ -196,6 +196,11 @@ LONG_ROW_CONFIGS = [
     {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "4", "LSE_WS_GROUP": "40", "LSE_WS_FW": "12"},
     {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "5", "LSE_WS_GROUP": "38", "LSE_WS_FW": "16"},
     {"LSE_LSM_VARIANT": "6", "LSE_WS_NB": "0", "LSE_WS_FW": "4", "LSE_WS_SW": "4"},
+    # warp-specialised group with a ring of chunk slots
+    {"LSE_LSM_VARIANT": "7"},
+    {"LSE_LSM_VARIANT": "7", "LSE_WS_GROUP": "19"},
+    {"LSE_LSM_VARIANT": "7", "LSE_WS_GROUP": "3", "LSE_RING_CHUNK": "4096"},
+    {"LSE_LSM_VARIANT": "7", "LSE_WS_GROUP": "40", "LSE_RING_CHUNK": "512"},
     # group with an L2 re-read
     {"LSE_LSM_VARIANT": "5"},
     {"LSE_LSM_VARIANT": "5", "LSE_L2_GROUP": "1"},

@@ -78,10 +78,11 @@ def test_softmax_parity(lib, cols):
     assert_parity(_softmax(lib, x), oracle.softmax(x), f"softmax cols={cols}")
 
 
-@pytest.mark.parametrize("variant", ["1", "3", "6", "2", "4", "5"])
+@pytest.mark.parametrize("variant", ["1", "3", "6", "7", "2", "4", "5"])
 def test_softmax_variants(lib, env, variant):
-    """Registers, streaming and warp-specialised kernels; the variants without a
-    softmax output fall back to the default choice."""
+    """Registers, streaming and warp-specialised kernels (whole-slice buffers or a ring
+    of chunk slots); the variants without a softmax output fall back to the default
+    choice."""
     env.setenv("LSE_LSM_VARIANT", variant)
     for rows, cols in ((7, 4096), (5, 393216), (3, 100003)):
         x = synth.normal((rows, cols), seed=rows * cols, var=9.0)
