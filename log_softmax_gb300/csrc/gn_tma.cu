@@ -14,7 +14,8 @@
 //                           (after a bounded wait for the sample's statistics);
 //                           each thread owns 4 adjacent pixels and either folds
 //                           the channel lse (OUT 0) or writes the GroupNorm
-//                           output (1) or y + hardswish(tanh(z)) (2).
+//                           output (1) or y + hardswish(tanh(z)) (2, as two
+//                           packed f32x2 pixel pairs).
 // A CTA keeps up to R chunks (R x 32 KB) in flight, so a few CTAs per SM hide
 // the HBM and L2 latency that per-thread loads could not.  The statistics
 // chunks ask L2 to keep their lines (the apply tiles of the same sample read
@@ -60,8 +61,11 @@ __global__ void __launch_bounds__(T) gn_tma_kernel(const GnTmaArgs a) {
     const int R = a.nslot;
     const int C = a.C, G = a.G, cpg = C / G;
     float* const ring = reinterpret_cast<float*>(smem_raw);                                   // [R][CF]
+    // OUT 2 takes the pair-form table [C] {mean, mean, sc, sc} then [C] {sh, sh};
+    // OUT 0 and 1 [C] {mean, rstd * gamma (* 2 log2 e for OUT 0), beta (likewise), 0}
     float4* const tab = reinterpret_cast<float4*>(smem_raw + (size_t)R * kGntSlotBytes);     // [C]
-    uint64_t* const full = reinterpret_cast<uint64_t*>(tab + C);                             // [R]
+    float2* const tab_b = reinterpret_cast<float2*>(tab + C);                                // [C]
+    uint64_t* const full = reinterpret_cast<uint64_t*>(tab_b + C);                           // [R]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t N = a.N, HW = a.HW;
     const int64_t GP = G, TT = a.tiles, lag = a.lag;
@@ -210,8 +214,12 @@ __global__ void __launch_bounds__(T) gn_tma_kernel(const GnTmaArgs a) {
                              : "l"(a.partials + n * G + g)
                              : "memory");
                 const float rstd = 1.f / sqrtf(q.z / q.x + a.eps);
-                const float kk = OUT == 1 ? 1.f : 2.f * kLog2e;
-                tab[c] = make_float4(q.y, rstd * a.gamma[c] * kk, a.beta[c] * kk, 0.f);
+                if constexpr (OUT == 2)
+                    gn_pair_entry(q.y, rstd * a.gamma[c] * (2.f * kLog2e), a.beta[c] * (2.f * kLog2e), tab, tab_b, c);
+                else {
+                    const float kk = OUT == 1 ? 1.f : 2.f * kLog2e;
+                    tab[c] = make_float4(q.y, rstd * a.gamma[c] * kk, a.beta[c] * kk, 0.f);
+                }
             }
             __syncthreads();
             const bool on = 4 * tid < tw;
@@ -254,15 +262,23 @@ __global__ void __launch_bounds__(T) gn_tma_kernel(const GnTmaArgs a) {
                     } else {
                         float* dst = a.out + (n * C + c0) * HW + px0 + 4 * tid;
                         for (int cc = 0; cc < nr; ++cc) {
-                            const float4 x = *reinterpret_cast<const float4*>(sl + cc * TP);
-                            const float4 e = tab[c0 + cc];
                             float4 o;
                             if constexpr (OUT == 1) {
+                                const float4 x = *reinterpret_cast<const float4*>(sl + cc * TP);
+                                const float4 e = tab[c0 + cc];
                                 o = make_float4(fmaf(x.x - e.x, e.y, e.z), fmaf(x.y - e.x, e.y, e.z),
                                                 fmaf(x.z - e.x, e.y, e.z), fmaf(x.w - e.x, e.y, e.z));
                             } else {
-                                o = make_float4(act_residual(x.x, e), act_residual(x.y, e), act_residual(x.z, e),
-                                                act_residual(x.w, e));
+                                // y + hardswish(tanh(z)) in pair form, plus the 2/3 it leaves out
+                                const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(sl + cc * TP);
+                                const float4 ta = tab[c0 + cc];
+                                const float2 tb = tab_b[c0 + cc];
+                                const f32x2 mean = f2_pack(ta.x, ta.y), sc = f2_pack(ta.z, ta.w);
+                                const f32x2 sh = f2_pack(tb.x, tb.y), k23 = f2_pack(2.f / 3.f, 2.f / 3.f);
+                                const f32x2 ra = f2_add(f2_residual_less_2_3(v.x, mean, sc, sh), k23);
+                                const f32x2 rb = f2_add(f2_residual_less_2_3(v.y, mean, sc, sh), k23);
+                                f2_unpack(ra, o.x, o.y);
+                                f2_unpack(rb, o.z, o.w);
                             }
                             st_stream_f4(dst + cc * HW, o);
                         }
@@ -292,9 +308,11 @@ size_t gn_tma_scratch_bytes(int64_t N, int64_t G) {
     return (size_t)N * G * sizeof(float4) + ((size_t)N * sizeof(unsigned) + 15) / 16 * 16 + 16;
 }
 
-// Shared memory of one CTA with `slots` ring slots.
+// Shared memory of one CTA with `slots` ring slots (the table takes 24 bytes per
+// channel, enough for the pair form).
 static size_t gn_tma_smem(int64_t C, int slots) {
-    return (size_t)slots * kGntSlotBytes + (size_t)C * sizeof(float4) + kGntMaxSlots * sizeof(uint64_t);
+    return (size_t)slots * kGntSlotBytes + (size_t)C * (sizeof(float4) + sizeof(float2)) +
+           kGntMaxSlots * sizeof(uint64_t);
 }
 
 bool gn_tma_applies(const DeviceInfo& dev, const float* y, const float* out, int64_t C, int64_t HW) {
