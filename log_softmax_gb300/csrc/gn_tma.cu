@@ -61,8 +61,8 @@ __global__ void __launch_bounds__(T) gn_tma_kernel(const GnTmaArgs a) {
     const int R = a.nslot;
     const int C = a.C, G = a.G, cpg = C / G;
     float* const ring = reinterpret_cast<float*>(smem_raw);                                   // [R][CF]
-    // OUT 2 takes the pair-form table [C] {mean, mean, sc, sc} then [C] {sh, sh};
-    // OUT 0 and 1 [C] {mean, rstd * gamma (* 2 log2 e for OUT 0), beta (likewise), 0}
+    // OUT 0 and 2 take the pair-form table [C] {mean, mean, sc, sc} then [C] {sh, sh};
+    // OUT 1 [C] {mean, rstd * gamma, beta, 0}
     float4* const tab = reinterpret_cast<float4*>(smem_raw + (size_t)R * kGntSlotBytes);     // [C]
     float2* const tab_b = reinterpret_cast<float2*>(tab + C);                                // [C]
     uint64_t* const full = reinterpret_cast<uint64_t*>(tab_b + C);                           // [R]
@@ -214,18 +214,14 @@ __global__ void __launch_bounds__(T) gn_tma_kernel(const GnTmaArgs a) {
                              : "l"(a.partials + n * G + g)
                              : "memory");
                 const float rstd = 1.f / sqrtf(q.z / q.x + a.eps);
-                if constexpr (OUT == 2)
+                if constexpr (OUT != 1)
                     gn_pair_entry(q.y, rstd * a.gamma[c] * (2.f * kLog2e), a.beta[c] * (2.f * kLog2e), tab, tab_b, c);
-                else {
-                    const float kk = OUT == 1 ? 1.f : 2.f * kLog2e;
-                    tab[c] = make_float4(q.y, rstd * a.gamma[c] * kk, a.beta[c] * kk, 0.f);
-                }
+                else
+                    tab[c] = make_float4(q.y, rstd * a.gamma[c], a.beta[c], 0.f);
             }
             __syncthreads();
             const bool on = 4 * tid < tw;
-            MS st[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) st[j] = ms_empty();
+            Lse4 st = lse4_empty();
             for (int i = 0; i < nck_apply; ++i) {
                 const uint64_t s = seq + i;
                 const int r = (int)(s % R);
@@ -234,29 +230,27 @@ __global__ void __launch_bounds__(T) gn_tma_kernel(const GnTmaArgs a) {
                 const float* sl = ring + (size_t)r * CF + 4 * tid;
                 if (on) {
                     if constexpr (OUT == 0) {
+                        // the chain's residual in pair form (less 2/3), folded into the
+                        // running channel lse of this thread's four pixels
+                        auto residual = [&](int cc, f32x2& ra, f32x2& rb) {
+                            const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(sl + cc * TP);
+                            const float4 ta = tab[c0 + cc];
+                            const float2 tb = tab_b[c0 + cc];
+                            const f32x2 mean = f2_pack(ta.x, ta.y), sc = f2_pack(ta.z, ta.w);
+                            const f32x2 sh = f2_pack(tb.x, tb.y);
+                            ra = f2_residual_less_2_3(v.x, mean, sc, sh);
+                            rb = f2_residual_less_2_3(v.y, mean, sc, sh);
+                        };
                         if (nr == CC) {
-                            float v[4][CC];
+                            f32x2 ra[CC], rb[CC];
 #pragma unroll
-                            for (int cc = 0; cc < CC; ++cc) {
-                                const float4 x = *reinterpret_cast<const float4*>(sl + cc * TP);
-                                const float4 e = tab[c0 + cc];
-                                v[0][cc] = act_residual(x.x, e);
-                                v[1][cc] = act_residual(x.y, e);
-                                v[2][cc] = act_residual(x.z, e);
-                                v[3][cc] = act_residual(x.w, e);
-                            }
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) ms_fold<CC>(st[j], v[j]);
+                            for (int cc = 0; cc < CC; ++cc) residual(cc, ra[cc], rb[cc]);
+                            lse4_fold<CC>(st, ra, rb);
                         } else {
                             for (int cc = 0; cc < nr; ++cc) {
-                                const float4 x = *reinterpret_cast<const float4*>(sl + cc * TP);
-                                const float4 e = tab[c0 + cc];
-                                float v0[1] = {act_residual(x.x, e)}, v1[1] = {act_residual(x.y, e)};
-                                float v2[1] = {act_residual(x.z, e)}, v3[1] = {act_residual(x.w, e)};
-                                ms_fold<1>(st[0], v0);
-                                ms_fold<1>(st[1], v1);
-                                ms_fold<1>(st[2], v2);
-                                ms_fold<1>(st[3], v3);
+                                f32x2 ra[1], rb[1];
+                                residual(cc, ra[0], rb[0]);
+                                lse4_fold<1>(st, ra, rb);
                             }
                         }
                     } else {
@@ -289,9 +283,13 @@ __global__ void __launch_bounds__(T) gn_tma_kernel(const GnTmaArgs a) {
             }
             seq += nck_apply;
             if constexpr (OUT == 0) {
-                if (on)
+                if (on) {
+                    float m[4], sm[4];
+                    lse4_unpack(st, m, sm);
                     *reinterpret_cast<float4*>(a.out + n * HW + px0 + 4 * tid) =
-                        make_float4(ms_lse(st[0]), ms_lse(st[1]), ms_lse(st[2]), ms_lse(st[3]));
+                        make_float4(m[0] + logf(sm[0]) + 2.f / 3.f, m[1] + logf(sm[1]) + 2.f / 3.f,
+                                    m[2] + logf(sm[2]) + 2.f / 3.f, m[3] + logf(sm[3]) + 2.f / 3.f);
+                }
             }
         }
     }
