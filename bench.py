@@ -10,7 +10,7 @@ rank runs the whole workload on its own GPU (independent batches, weak
 scaling) with no data-path collective; the timed region is bracketed by a
 barrier and a device synchronize, and the slowest rank's time is reported.
 
-On one GPU the line also carries `configs`: every other workload of the path
+On one GPU, for the default workload, the line also carries `configs`: every other workload of the path
 (the logsumexp over dim 0 and log_softmax cases, the GroupNorm chain, and the
 operations beside them) measured in the same run after the default one, each
 with its time per call and its fraction of the HBM (or tf32 tensor) peak.
@@ -890,9 +890,9 @@ def run_ours(args, w: synth.Workload):
         except Exception as e:  # the single-threaded figure stands alone
             cpu["all_cores"] = {"unavailable": repr(e)[:200]}
 
-    # the other workloads of the path, measured in this same run (one GPU only)
+    # the other workloads of the path, measured in this same run (one GPU, default workload)
     configs = None
-    if rank == 0 and world == 1 and not args.no_configs and not args.shape:
+    if rank == 0 and world == 1 and not args.no_configs and w.name == DEFAULT_WORKLOAD:
         del inputs, out, flush, step
         torch.cuda.empty_cache()
         configs = {}
