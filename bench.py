@@ -92,9 +92,9 @@ GN_ELEMENTWISE = ("group_norm", "gn_act_residual")
 # Kernels each step launches (the dominant kernel first).
 LAUNCHES = {
     "lse_dim0": ["lse_strided_kernel"],
-    "log_softmax": ["lsm_ws_kernel"],
+    "log_softmax": ["lsm_tmem_kernel"],
     "gn_act_lse": ["gn_fused_kernel"],
-    "softmax": ["lsm_ws_kernel"],
+    "softmax": ["lsm_tmem_kernel"],
     "log_softmax_dim0": ["lse_strided_kernel"],
     "group_norm": ["gn_tma_kernel"],
     "gn_act_residual": ["gn_tma_kernel"],
@@ -261,7 +261,7 @@ def gn_chain_sfu_clocks_per_element() -> float:
 
 # The sources that determine each dominant kernel's code (with the shared headers).
 KERNEL_SOURCES = {
-    "lsm_ws_kernel": ["log_softmax.cu"],
+    "lsm_tmem_kernel": ["log_softmax.cu"],
     "lse_strided_kernel": ["lse_strided.cu"],
     "gn_fused_kernel": ["gn_act_lse.cu", "gn_common.cuh"],
     "gn_tma_kernel": ["gn_tma.cu", "gn_common.cuh"],

@@ -49,7 +49,10 @@
  * the tolerance above):
  *   - Kernel choice: LSE_LSM_VARIANT (rows: 1 registers, 2 cluster shared
  *     memory, 3 streaming, 4 lock-step group, 5 group with an L2 re-read,
- *     6 warp-specialised group; default by shape), LSE_GN_VARIANT (GroupNorm
+ *     6 warp-specialised group with whole-slice shared-memory buffers, 7 the
+ *     same with a ring of chunk slots, 8 the same with the rows parked in
+ *     tensor memory; default by shape: 1 up to 32768 columns, else 8, else 6,
+ *     else 3), LSE_GN_VARIANT (GroupNorm
  *     forms: 1 statistics kernel then apply kernel (gn_act_lse only), 2 work
  *     queue with per-thread loads, 3 work queue with bulk-copy staging, 4 sample
  *     slices held in shared memory by groups of CTAs, y read once (gn_act_lse
@@ -62,7 +65,9 @@
  *     LSE_STRIDED_ONE_WALK (0: the strided log_softmax always walks a tile
  *     twice).
  *   - Tuning: LSE_WS_GROUP / LSE_WS_NB / LSE_WS_FW / LSE_WS_SW (warp-
- *     specialised rows: CTAs per row, buffers, fold and store warps),
+ *     specialised rows: CTAs per row, buffers, fold and store warps;
+ *     LSE_WS_GROUP also for 7 and 8), LSE_RING_CHUNK / LSE_TMEM_CHUNK (floats
+ *     per landing chunk of 7 and 8),
  *     LSE_LSM_CLUSTER / LSE_LSM_GROUP / LSE_LSM_THREADS / LSE_LSM_NBUF /
  *     LSE_LSM_CHUNK, LSE_L2_GROUP / LSE_L2_THREADS, LSE_STREAM_CLUSTER (the
  *     other row kernels), LSE_GN_THREADS / LSE_GN_PARTS / LSE_GN_LAG /

@@ -66,6 +66,14 @@ cudaError_t plan_lsm_ring_group(const DeviceInfo& dev, const float* x, const flo
 cudaError_t launch_lsm_ring_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows, int64_t cols,
                                   const GroupPlan& plan, void* scratch, cudaStream_t stream, bool softmax = false);
 
+// Form 2, the warp-specialised group kernel with its rows parked in tensor memory
+// while their lse is merged (shared memory holds landing chunks only); plan.nbuf holds
+// 100 x landing slots + tensor-memory row buffers.  Same plan / scratch protocol.
+cudaError_t plan_lsm_tmem_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
+                                int64_t cols, GroupPlan* plan);
+cudaError_t launch_lsm_tmem_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows, int64_t cols,
+                                  const GroupPlan& plan, void* scratch, cudaStream_t stream, bool softmax = false);
+
 // Form 2, rows split over a group of CTAs of a cooperative grid that read their
 // slices twice, the second time from L2.  Same plan / scratch protocol.
 cudaError_t plan_lsm_l2_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,

@@ -203,24 +203,30 @@ lse_status_t row_transform(const float* x, float* out, int64_t rows, int64_t col
     cudaError_t e;
     // LSE_LSM_VARIANT forces a kernel: 1 registers, 2 cluster shared memory,
     // 3 streaming, 4 lock-step group shared memory, 5 group with an L2 re-read,
-    // 6 warp-specialised group shared memory (the default for long aligned rows),
-    // 7 the same with a ring of chunk slots per CTA.  softmax has the register,
+    // 6 warp-specialised group shared memory, 7 the same with a ring of chunk slots
+    // per CTA, 8 the same with its rows parked in tensor memory (the default for long
+    // 16-byte-aligned rows; 6 where 8 has no plan).  softmax has the register,
     // streaming and warp-specialised kernels only.
     int force = env_int("LSE_LSM_VARIANT", 0);
-    if (softmax && force != 1 && force != 3 && force != 6 && force != 7) force = 0;
+    if (softmax && force != 1 && force != 3 && force != 6 && force != 7 && force != 8) force = 0;
     if ((force == 0 || force == 1) && cols <= kRegRowMaxCols) {
         e = launch_rows_reg(s->info, x, out, rows, cols, softmax ? 2 : 0, stream);
     } else {
         e = cudaErrorNotSupported;
         if (force == 2) {
             e = launch_lsm_smem_cluster(s->info, x, out, rows, cols, stream);
-        } else if (force == 0 || force == 4 || force == 5 || force == 6 || force == 7) {
-            const int kind = force == 0 ? 6 : force;
+        } else if (force == 0 || (force >= 4 && force <= 8)) {
             GroupPlan plan;
-            e = kind == 5 ? plan_lsm_l2_group(s->info, x, out, rows, cols, &plan)
-              : kind == 6 ? plan_lsm_ws_group(s->info, x, out, rows, cols, &plan)
-              : kind == 7 ? plan_lsm_ring_group(s->info, x, out, rows, cols, &plan)
-                          : plan_lsm_smem_group(s->info, x, out, rows, cols, &plan);
+            auto plan_kind = [&](int kind) {
+                return kind == 5 ? plan_lsm_l2_group(s->info, x, out, rows, cols, &plan)
+                     : kind == 6 ? plan_lsm_ws_group(s->info, x, out, rows, cols, &plan)
+                     : kind == 7 ? plan_lsm_ring_group(s->info, x, out, rows, cols, &plan)
+                     : kind == 8 ? plan_lsm_tmem_group(s->info, x, out, rows, cols, &plan)
+                                 : plan_lsm_smem_group(s->info, x, out, rows, cols, &plan);
+            };
+            int kind = force == 0 ? 8 : force;
+            e = plan_kind(kind);
+            if (e == cudaErrorNotSupported && force == 0) e = plan_kind(kind = 6);
             if (e == cudaSuccess) {
                 cudaMemPool_t pool = nullptr;
                 if ((st = device_pool(s, &pool)) != LSE_OK) return st;
@@ -230,6 +236,7 @@ lse_status_t row_transform(const float* x, float* out, int64_t rows, int64_t col
                 e = kind == 5 ? launch_lsm_l2_group(s->info, x, out, rows, cols, plan, scratch, stream)
                   : kind == 6 ? launch_lsm_ws_group(s->info, x, out, rows, cols, plan, scratch, stream, softmax)
                   : kind == 7 ? launch_lsm_ring_group(s->info, x, out, rows, cols, plan, scratch, stream, softmax)
+                  : kind == 8 ? launch_lsm_tmem_group(s->info, x, out, rows, cols, plan, scratch, stream, softmax)
                               : launch_lsm_smem_group(s->info, x, out, rows, cols, plan, scratch, stream);
                 cudaError_t ef = cudaFreeAsync(scratch, stream);
                 if (e == cudaSuccess) e = ef;

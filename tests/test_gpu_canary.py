@@ -45,7 +45,7 @@ def _intact(buf, pad, n):
 
 @pytest.mark.parametrize("shift", [0, 1])
 def test_row_ops(lib, shift, monkeypatch):
-    for variant in ("0", "7", "3", "1"):
+    for variant in ("0", "7", "8", "3", "1"):
         monkeypatch.setenv("LSE_LSM_VARIANT", variant)
         for rows, cols in ((3, 5), (7, 4099), (5, 70001), (3, 393216)):
             x = synth.normal((rows, cols), seed=rows + cols)

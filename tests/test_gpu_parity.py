@@ -201,6 +201,11 @@ LONG_ROW_CONFIGS = [
     {"LSE_LSM_VARIANT": "7", "LSE_WS_GROUP": "19"},
     {"LSE_LSM_VARIANT": "7", "LSE_WS_GROUP": "3", "LSE_RING_CHUNK": "4096"},
     {"LSE_LSM_VARIANT": "7", "LSE_WS_GROUP": "40", "LSE_RING_CHUNK": "512"},
+    # warp-specialised group with its rows parked in tensor memory
+    {"LSE_LSM_VARIANT": "8"},
+    {"LSE_LSM_VARIANT": "8", "LSE_WS_GROUP": "19"},
+    {"LSE_LSM_VARIANT": "8", "LSE_WS_GROUP": "3", "LSE_TMEM_CHUNK": "4096"},
+    {"LSE_LSM_VARIANT": "8", "LSE_WS_GROUP": "40", "LSE_TMEM_CHUNK": "1024"},
     # group with an L2 re-read
     {"LSE_LSM_VARIANT": "5"},
     {"LSE_LSM_VARIANT": "5", "LSE_L2_GROUP": "1"},

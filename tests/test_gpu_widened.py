@@ -78,7 +78,7 @@ def test_softmax_parity(lib, cols):
     assert_parity(_softmax(lib, x), oracle.softmax(x), f"softmax cols={cols}")
 
 
-@pytest.mark.parametrize("variant", ["1", "3", "6", "7", "2", "4", "5"])
+@pytest.mark.parametrize("variant", ["1", "3", "6", "7", "8", "2", "4", "5"])
 def test_softmax_variants(lib, env, variant):
     """Registers, streaming and warp-specialised kernels (whole-slice buffers or a ring
     of chunk slots); the variants without a softmax output fall back to the default
