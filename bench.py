@@ -261,7 +261,7 @@ def gn_chain_sfu_clocks_per_element() -> float:
 
 # The sources that determine each dominant kernel's code (with the shared headers).
 KERNEL_SOURCES = {
-    "lsm_tmem_kernel": ["log_softmax.cu"],
+    "lsm_tmem_kernel": ["log_softmax.cu", "tmem.cuh"],
     "lse_strided_kernel": ["lse_strided.cu"],
     "gn_fused_kernel": ["gn_act_lse.cu", "gn_common.cuh"],
     "gn_tma_kernel": ["gn_tma.cu", "gn_common.cuh"],

@@ -56,7 +56,9 @@
  *     forms: 1 statistics kernel then apply kernel (gn_act_lse only), 2 work
  *     queue with per-thread loads, 3 work queue with bulk-copy staging, 4 sample
  *     slices held in shared memory by groups of CTAs, y read once (gn_act_lse
- *     only, HW % 4 == 0, C <= 256, G <= 64; falls back otherwise); default 2
+ *     only, HW % 4 == 0, C <= 256, G <= 64; falls back otherwise), 5 a queue
+ *     of 256-pixel tiles parked in tensor memory, y read once (gn_act_lse
+ *     only, HW % 4 == 0, C % 4 == 0, C <= 64; falls back otherwise); default 2
  *     for gn_act_lse, 3 for group_norm and gn_act_residual),
  *     LSE_CONV_CHAIN (conv_gn_act_lse: 1 y and its tiles' statistics from
  *     the convolution's epilogue, then merge and apply; 2 y never in memory;
@@ -73,7 +75,9 @@
  *     other row kernels), LSE_GN_THREADS / LSE_GN_PARTS / LSE_GN_LAG /
  *     LSE_GN_CTAS_PER_SM and LSE_GNT_SLOTS / LSE_GNT_LAG / LSE_GNT_CTAS_PER_SM
  *     (the two GroupNorm work queues), LSE_SLAB_GROUP / LSE_SLAB_NB (CTAs per
- *     sample and slice buffers of the sample-slice kernel), LSE_HOST_CHUNK_MB (host pipeline chunk).
+ *     sample and slice buffers of the sample-slice kernel), LSE_GNM_SLOTS
+ *     (landing slots of the tensor-memory tile queue), LSE_HOST_CHUNK_MB (host
+ *     pipeline chunk).
  *   - LSE_VERBOSE=1 prints each launch's plan on stderr.
  *   - Test hooks, not for production: LSE_TEST_FAIL_ALLOC=1 makes every
  *     scratch allocation fail (the call returns LSE_ERR_CUDA and enqueues

@@ -45,6 +45,7 @@
 #include "common.cuh"
 #include "gn_common.cuh"
 #include "launch.h"
+#include "tmem.cuh"
 
 namespace lse {
 
@@ -133,17 +134,6 @@ __host__ __device__ inline int slab_row_readers(int G) {
     int t = 1;
     while (t < pairs) t <<= 1;
     return t < 32 ? t : 32;
-}
-
-// 2-D tensor copy of the box at (x, row) of `map` into shared memory, completing on
-// `bar` by transaction count; the source lines are marked evict-first (read once).
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int row, uint64_t* bar,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(row), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
 }
 
 template <int NBMAX>
@@ -412,11 +402,7 @@ static size_t gn_slab_smem(int C, int G, int P, int NB) {
 
 // cuTensorMapEncodeTiled from the driver, found once through the runtime (the library
 // does not link the driver library itself); null if unavailable.
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_tiled() {
+EncodeTiledFn encode_tiled() {
     static std::once_flag once;
     static EncodeTiledFn fn = nullptr;
     std::call_once(once, [] {

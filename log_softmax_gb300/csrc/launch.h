@@ -2,6 +2,7 @@
 // lse_api.cu validates arguments and picks a variant; these only launch.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -117,6 +118,31 @@ size_t gn_tma_scratch_bytes(int64_t N, int64_t G);
 cudaError_t launch_gn_tma(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
                           int64_t N, int64_t C, int64_t HW, int64_t G, float eps, void* scratch, cudaStream_t stream,
                           int out_kind);
+
+// cuTensorMapEncodeTiled from the driver, found once through the runtime (the library
+// does not link the driver library itself); null if unavailable.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled();
+
+// Form 3 with y read once and each tile parked in tensor memory (the channel lse
+// only): a work queue of 256-pixel tiles of all C channels, claimed in sample order;
+// each tile lands in shared memory (2-D tensor copy), its per-group moments are
+// folded and published, it is copied into tensor memory, and once its sample's
+// statistics are complete (the last tile's CTA builds the channel table) the chain
+// and the channel lse run from tensor memory.  gn_tmem_plan says whether it applies
+// (HW % 4 == 0, 4 <= C <= 64 with C % 4 == 0, 16-byte aligned y and out, enough tile
+// buffers for the deadlock bound) and sizes the launch and its scratch.
+struct GnTmemPlan {
+    int grid = 0, T = 0, TR = 0, R = 0, threads = 0;
+    size_t smem = 0, scratch_bytes = 0;
+};
+bool gn_tmem_plan(const DeviceInfo& dev, const float* y, const float* out, int64_t N, int64_t C, int64_t HW,
+                  int64_t G, GnTmemPlan* plan);
+cudaError_t launch_gn_tmem(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
+                           int64_t N, int64_t C, int64_t HW, int64_t G, float eps, const GnTmemPlan& plan,
+                           void* scratch, cudaStream_t stream);
 
 // Form 3 with y read once: each sample split by pixels over a group of CTAs that
 // keep their slices in shared memory and exchange per-group partial statistics

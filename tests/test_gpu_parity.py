@@ -301,6 +301,8 @@ GN_CONFIGS = [
     {"LSE_GN_VARIANT": "4"},                                    # sample slices in shared memory
     {"LSE_GN_VARIANT": "4", "LSE_SLAB_NB": "2"},
     {"LSE_GN_VARIANT": "4", "LSE_SLAB_GROUP": "2"},
+    {"LSE_GN_VARIANT": "5"},                                    # tiles parked in tensor memory
+    {"LSE_GN_VARIANT": "5", "LSE_GNM_SLOTS": "2"},
 ]
 
 
@@ -340,6 +342,39 @@ def test_gn_act_lse_non_finite(lib, env, variant):
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, 4, 1e-5), f"non-finite y, variant {variant}")
 
 
+@pytest.mark.parametrize("N,C,H,W,G", [
+    (3, 64, 33, 40, 16),    # 6 tiles, the last with 40 pixels
+    (2, 12, 16, 16, 3),     # 3 channel blocks: the two channel halves differ
+    (1, 4, 2, 2, 1),        # one block of four channels, one 4-pixel tile
+    (2, 32, 32, 32, 8),     # 8 tile buffers
+    (7, 64, 20, 20, 4),     # 16 channels per group
+    (6, 64, 126, 126, 16),  # the full image: 63 tiles per sample
+    (6000, 4, 16, 16, 2),   # ~40 tiles per CTA: the announcement ring wraps
+])
+def test_gn_tmem_shapes(lib, env, N, C, H, W, G):
+    """The tile queue with tiles parked in tensor memory on ragged and extreme shapes."""
+    env.setenv("LSE_GN_VARIANT", "5")
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))
+    got = lib.gn_act_lse_forward(inp["y"].to(DEV), inp["gamma"].to(DEV), inp["beta"].to(DEV), G, 1e-5)
+    ref = oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], G, 1e-5)
+    assert_parity(got, ref, f"gn tmem {N,C,H,W,G}")
+
+
+def test_gn_tmem_non_finite(lib, env):
+    """The non-finite samples of test_gn_act_lse_non_finite with 48 pixels (a multiple of
+    4, so that the tensor-memory kernel takes them): NaN samples stay NaN everywhere."""
+    env.setenv("LSE_GN_VARIANT", "5")
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(4, 16, 6, 8))
+    y = inp["y"].clone()
+    y[0, 5, 2, 3] = float("nan")
+    y[1, 1, 0, 0] = float("inf")
+    y[2, 10, 5, 6] = float("-inf")
+    got = lib.gn_act_lse_forward(y.to(DEV), inp["gamma"].to(DEV), inp["beta"].to(DEV), 4, 1e-5).cpu()
+    assert all(bool(torch.isnan(got[n]).all()) for n in range(3))
+    assert not bool(torch.isnan(got[3]).any())
+    assert_parity(got, oracle.gn_act_lse(y, inp["gamma"], inp["beta"], 4, 1e-5), "non-finite y, variant 5")
+
+
 @pytest.mark.parametrize("variant", ["0", "1", "2", "3"])
 @pytest.mark.parametrize("N,H,W,G", [(2, 3, 4, 512), (1, 2, 2, 8192), (2, 3, 3, 64)])
 def test_gn_max_channels(lib, env, variant, N, H, W, G):
@@ -359,9 +394,11 @@ def test_gn_max_channels(lib, env, variant, N, H, W, G):
                       f"{fn} C=8192 G={G} v{variant}")
 
 
-def test_gn_act_lse_wide_range(lib):
+@pytest.mark.parametrize("variant", ["0", "5"])
+def test_gn_act_lse_wide_range(lib, env, variant):
     """Large gamma and shifted data: z spans about [-60, 60] (tanh saturates),
     a non-zero mean exercises the statistics."""
+    env.setenv("LSE_GN_VARIANT", variant)
     N, C, H, W, G = 2, 16, 20, 20, 4
     y = synth.normal((N, C, H, W), seed=77, mean=30.0, var=25.0)
     gamma = synth.uniform((C,), seed=78, lo=-12.0, hi=12.0)
@@ -370,13 +407,16 @@ def test_gn_act_lse_wide_range(lib):
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-3), "gn wide")
 
 
-def test_gn_act_lse_large_mean_small_spread(lib):
+@pytest.mark.parametrize("variant", ["0", "5"])
+def test_gn_act_lse_large_mean_small_spread(lib, env, variant):
     """Groups whose mean (1e3) is 1e4 times their spread (std 0.1, so rstd ~ 10): z stays
-    accurate (the mean is subtracted before scaling), and the channel lse near 1e3 keeps
-    within the relative part of the tolerance despite the rounding of the exponent's
-    shift (m log2 e).  (Beyond a ratio of ~1e5 no fp32 GroupNorm is accurate: the mean
-    itself is only known to half an ulp, e.g. 5e-4 at 1e4.)"""
-    N, C, H, W, G = 2, 16, 12, 12, 4
+    accurate (the mean is subtracted before scaling, and the tile-queue kernel merges its
+    tiles' means relative to one of them), and the channel lse near 1e3 keeps within the
+    relative part of the tolerance despite the rounding of the exponent's shift
+    (m log2 e).  (Beyond a ratio of ~1e5 no fp32 GroupNorm is accurate: the mean itself
+    is only known to half an ulp, e.g. 5e-4 at 1e4.)  40 x 40 pixels: 7 tiles of 256."""
+    env.setenv("LSE_GN_VARIANT", variant)
+    N, C, H, W, G = 2, 16, 40, 40, 4
     y = synth.normal((N, C, H, W), seed=81, mean=1.0e3, var=1.0e-2)
     gamma = synth.uniform((C,), seed=82, lo=0.5, hi=1.5)
     beta = synth.normal((C,), seed=83, var=0.1)
@@ -384,11 +424,13 @@ def test_gn_act_lse_large_mean_small_spread(lib):
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-5), "gn mean 1e3, std 0.1")
 
 
+@pytest.mark.parametrize("variant", ["0", "5"])
 @pytest.mark.parametrize("scale", [1.0e3, 1.0e6, 1.0e15])
-def test_gn_act_lse_large_values(lib, scale):
+def test_gn_act_lse_large_values(lib, env, scale, variant):
     """y of magnitude up to 1e15 with channels far apart: the running max and its
-    rescale carry the channel lse (terms span many binades)."""
-    N, C, H, W, G = 2, 24, 8, 8, 6
+    rescale carry the channel lse (terms span many binades).  32 x 32 pixels: 4 tiles."""
+    env.setenv("LSE_GN_VARIANT", variant)
+    N, C, H, W, G = 2, 24, 32, 32, 6
     y = synth.normal((N, C, H, W), seed=84) * scale
     gamma = synth.uniform((C,), seed=85, lo=0.5, hi=1.5)
     beta = synth.normal((C,), seed=86, var=0.1)
@@ -396,9 +438,12 @@ def test_gn_act_lse_large_values(lib, scale):
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-5), f"gn scale {scale}")
 
 
-def test_gn_act_lse_constant_group(lib):
-    """Zero variance in a group: z = beta exactly (eps keeps rstd finite)."""
-    y = torch.full((1, 4, 3, 3), 2.0)
+@pytest.mark.parametrize("variant", ["0", "5"])
+def test_gn_act_lse_constant_group(lib, env, variant):
+    """Zero variance in a group: z = beta exactly (eps keeps rstd finite).  20 x 20
+    pixels: two tiles, whose merged M2 stays exactly 0."""
+    env.setenv("LSE_GN_VARIANT", variant)
+    y = torch.full((1, 4, 20, 20), 2.0)
     gamma = torch.ones(4)
     beta = torch.tensor([0.0, 0.5, -1.0, 2.0])
     got = lib.gn_act_lse_forward(y.to(DEV), gamma.to(DEV), beta.to(DEV), 2, 1e-5)
