@@ -92,12 +92,12 @@ GN_ELEMENTWISE = ("group_norm", "gn_act_residual")
 # Kernels each step launches (the dominant kernel first).
 LAUNCHES = {
     "lse_dim0": ["lse_strided_kernel"],
-    "log_softmax": ["lsm_tmem_kernel"],
+    "log_softmax": ["row_tmem_kernel"],
     "gn_act_lse": ["gn_fused_kernel"],
-    "softmax": ["lsm_tmem_kernel"],
+    "softmax": ["row_tmem_kernel"],
     "log_softmax_dim0": ["lse_strided_kernel"],
-    "group_norm": ["gn_tma_kernel"],
-    "gn_act_residual": ["gn_tma_kernel"],
+    "group_norm": ["row_tmem_kernel"],
+    "gn_act_residual": ["row_tmem_kernel"],
     "conv_gn_act_lse": ["conv2d_tc_kernel", "gn_fused_kernel"],
 }
 
@@ -261,7 +261,7 @@ def gn_chain_sfu_clocks_per_element() -> float:
 
 # The sources that determine each dominant kernel's code (with the shared headers).
 KERNEL_SOURCES = {
-    "lsm_tmem_kernel": ["log_softmax.cu", "tmem.cuh"],
+    "row_tmem_kernel": ["row_tmem.cuh", "tmem.cuh", "log_softmax.cu", "gn_rows.cu", "gn_common.cuh"],
     "lse_strided_kernel": ["lse_strided.cu"],
     "gn_fused_kernel": ["gn_act_lse.cu", "gn_common.cuh"],
     "gn_tma_kernel": ["gn_tma.cu", "gn_common.cuh"],

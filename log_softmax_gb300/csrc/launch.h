@@ -119,6 +119,16 @@ cudaError_t launch_gn_tma(const DeviceInfo& dev, const float* y, const float* ga
                           int64_t N, int64_t C, int64_t HW, int64_t G, float eps, void* scratch, cudaStream_t stream,
                           int out_kind);
 
+// GroupNorm and the chain before the lse (out_kind 1 / 2) as rows of the tensor-memory
+// row kernel: the N x G slabs of C / G x HW floats, each read once and written once
+// (HW % 4 == 0, 16-byte aligned y and out; the default for these outputs where it
+// applies).  Same plan / scratch protocol as plan_lsm_tmem_group.
+cudaError_t plan_gn_rows(const DeviceInfo& dev, const float* y, const float* out, int64_t N, int64_t C, int64_t HW,
+                         int64_t G, int out_kind, GroupPlan* plan);
+cudaError_t launch_gn_rows(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
+                           int64_t N, int64_t C, int64_t HW, int64_t G, float eps, const GroupPlan& plan,
+                           void* scratch, cudaStream_t stream, int out_kind);
+
 // cuTensorMapEncodeTiled from the driver, found once through the runtime (the library
 // does not link the driver library itself); null if unavailable.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

@@ -50,6 +50,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "row_tmem.cuh"
 #include "tmem.cuh"
 
 namespace lse {
@@ -219,23 +220,6 @@ struct SmemRowArgs {
     int ring;                  // ring / tensor-memory kernels: chunk slots of shared memory per CTA
     int trows;                 // tensor-memory kernel: row buffers in tensor memory
 };
-
-// Polls a tagged slot until its tag is `tag`, at most ~1 s / 2^26 polls; on
-// timeout records kStatusTimeout and sets `aborted`.
-__device__ __forceinline__ unsigned long long poll_slot(const unsigned long long* p, uint32_t tag,
-                                                        unsigned long long w, bool& aborted, int* status) {
-    if (ms_tag_of(w) == tag || aborted) return w;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0; it < (1u << 26); ++it) {
-        __nanosleep(20);
-        w = ld_relaxed_gpu_u64(p);
-        if (ms_tag_of(w) == tag) return w;
-        if ((it & 255u) == 255u && globaltimer_ns() - t0 > 1000000000ull) break;
-    }
-    aborted = true;
-    atomicExch(status, kStatusTimeout);
-    return w;
-}
 
 // Rows staged in shared memory, one slice per CTA, the CTAs of a row merging
 // their (m, s) pairs either through distributed shared memory (GROUP = false:
@@ -769,283 +753,33 @@ __global__ void __launch_bounds__(32 * (FW + SW), 1) lsm_ring_kernel(const SmemR
     }
 }
 
-// ---- rows parked in tensor memory while their lse is merged
+// ---- rows parked in tensor memory while their lse is merged (row_tmem.cuh)
 
-constexpr int kTmemCols = 512;
-constexpr int kTmemMaxRows = 7;  // rows parked per CTA; 2 x 7 < kWsSlots keeps the pair slots safe
-constexpr int kTmemLseRing = 8;  // row lse values handed from the merge warp to the store warps (> kTmemMaxRows)
-constexpr int kTmemMinSlice = 16384;  // floats of a CTA's slice below which the group round trip dominates
-
-// lsm_tmem_kernel: lsm_ws_kernel's roles with the rows parked in tensor memory, and
-// the copies in warps of their own so that no fold warp waits on them.
-//   fold warps   fold each landed chunk (shared-memory slot g % R, chunk g = j * nch + c of
-//                the CTA) into the row's pair and arrive on folded[slot]; at the end of a
-//                row they publish its pair through the tagged group slots as in
-//                lsm_ws_kernel.
-//   copy warp    once a chunk is folded, copies it into row buffer j % TR of tensor
-//                memory (after the store warps have released that buffer's previous
-//                row) and commits the copy to freed[slot] (and, for the row's last
-//                chunk, to tready[buffer]).
-//   load warp    issues every bulk copy: chunk g + R into slot g % R once chunk g's
-//                tensor-memory copy has completed.
-//   merge warp   waits for this CTA's own pair of a row (pub), merges the group's
-//                pairs into its lse and hands it over through lse_s[j % 8] and
-//                lse_full[j % 8], so that the stores never wait for a round trip to L2
-//                and no warp polls L2 for a row long before it can be complete.
-//   store warps  wait for the row's lse and its copies (tready), read their lanes of
-//                the row buffer, write x - lse (or its exponential), and release the
-//                buffer (tfree, one arrival per warp).
-// Shared memory then holds only chunks in flight from HBM, being folded or being
-// copied, and up to TR rows wait for their lse in tensor memory.  Fold warp 0
-// publishes row r only after this CTA's store of row r - TR, which implies every CTA's
-// pairs of r - TR, hence every CTA's store (and, the merge warp taking rows in order,
-// every CTA's merge) of r - 2 TR: 2 TR < kWsSlots keeps the tagged slots safe.
-// The merge of row r in turn needs this CTA's store of r - TR, so lse_s[r % 8] is
-// never overwritten before it has been read, and pub[r % 8] completes again only after
-// the merge of r (TR < 8).  Waits are bounded.
-template <int FW, int SW>
-__global__ void __launch_bounds__(32 * (FW + SW + 3), 1) lsm_tmem_kernel(const SmemRowArgs a) {
-    static_assert(SW == 4, "one store warp per quarter of the tensor-memory lanes");
-    static_assert(kTmemMaxRows < kTmemLseRing && 2 * kTmemMaxRows < kWsSlots, "hand-over rings too small");
-    constexpr int NF = 32 * FW;
-    constexpr int kCopyWarp = FW + SW, kLoadWarp = FW + SW + 1, kMergeWarp = FW + SW + 2;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    const int chunk = a.chunk, R = a.ring, TR = a.trows;
-    const int64_t rows = a.rows, cols = a.cols;
-    float* const ring = reinterpret_cast<float*>(smem_raw);                                      // [R][chunk]
-    uint64_t* const full = reinterpret_cast<uint64_t*>(smem_raw + (size_t)R * chunk * 4);       // [kRingMax]
-    uint64_t* const freed = full + kRingMax;                                                    // [kRingMax]
-    uint64_t* const folded = freed + kRingMax;                                                  // [kRingMax]
-    uint64_t* const tfree = folded + kRingMax;                                                  // [kTmemMaxRows]
-    uint64_t* const tready = tfree + kTmemMaxRows;                                              // [kTmemMaxRows]
-    uint64_t* const lse_full = tready + kTmemMaxRows;                                           // [kTmemLseRing]
-    uint64_t* const pub = lse_full + kTmemLseRing;                                              // [kTmemLseRing]
-    long long* const copied_s = reinterpret_cast<long long*>(pub + kTmemLseRing);               // [1]
-    float* const lse_s = reinterpret_cast<float*>(copied_s + 1);                                // [kTmemLseRing]
-    uint32_t* const tslot = reinterpret_cast<uint32_t*>(lse_s + kTmemLseRing);                  // [1]
-    MS* const red = reinterpret_cast<MS*>(lse_s + kTmemLseRing + 2);                            // [2][32]
-
-    const uint32_t GS = (uint32_t)a.group_size;
-    const uint32_t rank = blockIdx.x % GS;
-    const int64_t first_row = blockIdx.x / GS;
-    const int64_t row_step = gridDim.x / GS;
-    unsigned long long* const slots = a.slots + first_row * kWsSlots * GS;  // [kWsSlots][GS]
-    const int64_t c_begin = (int64_t)rank * a.slice;
-    const int len = (int)std::max<int64_t>(0, std::min<int64_t>(a.slice, cols - c_begin));
-    const int nch = (len + chunk - 1) / chunk;
-    const int cpr = (a.slice + 1023) / 1024 * 8;  // tensor-memory columns of one row buffer
-    const int64_t nrows = first_row < rows ? (rows - first_row + row_step - 1) / row_step : 0;
-    const int64_t total = nrows * nch;
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    bool aborted = false;
-
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    if (tid == 0) {
-        for (int r = 0; r < R; ++r) {
-            mbar_init(&full[r], 1);
-            mbar_init(&freed[r], 1);
-            mbar_init(&folded[r], FW);
-        }
-        for (int b = 0; b < TR; ++b) {
-            mbar_init(&tfree[b], SW);
-            mbar_init(&tready[b], 1);
-        }
-        for (int k = 0; k < kTmemLseRing; ++k) {
-            mbar_init(&lse_full[k], 1);
-            mbar_init(&pub[k], 1);
-        }
-        *copied_s = 0;
-        fence_mbar_init();
-    }
-    tmem_fence_before();
-    __syncthreads();
-    tmem_fence_after();
-    const uint32_t tbase = *tslot;
-
-    int64_t issued = 0;  // load warp: chunks whose bulk copy has been issued
-    auto issue = [&](int64_t g) {
-        const int64_t j = g / nch;
-        const int c = (int)(g - j * nch);
-        const int sl = (int)(g % R);
-        const int cb = c * chunk;
-        const uint32_t bytes = (uint32_t)std::min(chunk, len - cb) * 4u;
-        mbar_arrive_expect_tx(&full[sl], bytes);
-        bulk_g2s(ring + (size_t)sl * chunk, a.x + (first_row + j * row_step) * cols + c_begin + cb, bytes, &full[sl]);
-        issued = g + 1;
+// The row statistic of log_softmax / softmax for the tensor-memory row kernel: the
+// (max, sum of exponentials) pair, the row's lse, and x - lse or its exponential.
+struct LsmOp {
+    struct Params {
+        int softmax;
     };
-
-    if (warp < FW) {
-        // ---------------- fold warps
-        for (int64_t j = 0; j < nrows; ++j) {
-            MS st = ms_empty();
-            for (int c = 0; c < nch; ++c) {
-                const int64_t g = j * nch + c;
-                const int sl = (int)(g % R);
-                mbar_wait_bounded(&full[sl], (uint32_t)((g / R) & 1), aborted, a.status);
-                const int n = std::min(chunk, len - c * chunk);
-                const int n4 = n >> 2;
-                const float4* p = reinterpret_cast<const float4*>(ring + (size_t)sl * chunk);
-                int i = tid;
-                for (; i + 3 * NF < n4; i += 4 * NF) {
-                    float v[16];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float4 q = p[i + k * NF];
-                        v[4 * k + 0] = q.x; v[4 * k + 1] = q.y; v[4 * k + 2] = q.z; v[4 * k + 3] = q.w;
-                    }
-                    ms_fold<16>(st, v);
-                }
-                for (; i < n4; i += NF) {
-                    float4 q = p[i];
-                    float v[4] = {q.x, q.y, q.z, q.w};
-                    ms_fold<4>(st, v);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&folded[sl]);  // this warp is done reading slot sl
-            }
-            st = ms_warp_allreduce(st);
-            if (lane == 0) red[(j & 1) * 32 + warp] = st;
-            named_bar_sync(1, NF);  // every fold warp is done with this row and its red slot
-            if (warp == 0) {
-                MS r = (lane < FW) ? red[(j & 1) * 32 + lane] : ms_empty();
-                r = ms_warp_allreduce(r);
-                // Not before this CTA's store of row j - TR: that bounds how far the pairs
-                // run ahead of every CTA's reads of the tagged slots (the fold warps alone
-                // could run R / nch + TR rows ahead).  The phase cannot move on before
-                // this publication, since it is the next use of the buffer.
-                if (j >= TR)
-                    mbar_wait_bounded(&tfree[j % TR], (uint32_t)(((j - TR) / TR) & 1), aborted, a.status);
-                if (lane == 0) {
-                    st_relaxed_gpu_u64(slots + (j % kWsSlots) * GS + rank,
-                                       ms_pack_tagged(r, (uint32_t)(j / kWsSlots) & 1u));
-                    mbar_arrive(&pub[j % kTmemLseRing]);
-                }
-            }
-        }
-    } else if (warp < FW + SW) {
-        // ---------------- store warps: read the row from tensor memory, write
-        const uint32_t quarter = (uint32_t)(warp & 3);  // the lanes this warp may read
-        const int l = (int)quarter * 32 + lane;          // tensor-memory lane of this thread
-        for (int64_t j = 0; j < nrows; ++j) {
-            const int b = (int)(j % TR);
-            mbar_wait_bounded(&lse_full[j % kTmemLseRing], (uint32_t)((j / kTmemLseRing) & 1), aborted, a.status);
-            const float lse = lse_s[j % kTmemLseRing];
-            mbar_wait_bounded(&tready[b], (uint32_t)((j / TR) & 1), aborted, a.status);
-            tmem_fence_after();
-            float* dst = a.out + (first_row + j * row_step) * cols + c_begin;
-            const int nblk = (len + 1023) / 1024;
-            const uint32_t taddr = tbase + (quarter << 21) + (uint32_t)(b * cpr);  // lane field: 32 q << 16
-            // one block: lane l's floats [4l, 4l + 4) and [512 + 4l, 512 + 4l + 4) of it
-            auto put = [&](int k, const uint32_t* r) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int e = 1024 * k + 512 * h + 4 * l;
-                    if (e < len) {
-                        const float4 q = make_float4(__uint_as_float(r[4 * h + 0]), __uint_as_float(r[4 * h + 1]),
-                                                     __uint_as_float(r[4 * h + 2]), __uint_as_float(r[4 * h + 3]));
-                        st_stream_f4(dst + e, row_out4(q, lse, a.softmax != 0));
-                    }
-                }
-            };
-            int k0 = 0;
-            for (; k0 + 4 <= nblk; k0 += 4) {  // four blocks per load; never past the row's columns
-                uint32_t r[32];
-                tmem_ld32(taddr + 8u * k0, r);
-                tmem_wait_ld_all();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) put(k0 + kk, r + 8 * kk);
-            }
-            for (; k0 < nblk; ++k0) {
-                uint32_t r[8];
-                tmem_ld8(taddr + 8u * k0, r);
-                tmem_wait_ld_all();
-                put(k0, r);
-            }
-            tmem_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tfree[b]);
-        }
-    } else if (warp == kCopyWarp) {
-        // ---------------- copy warp: folded chunks into tensor memory
-        if (lane == 0) {
-            int64_t copied = 0;
-            for (int64_t g = 0; g < total && !aborted; ++g) {
-                const int64_t j = g / nch;
-                const int c = (int)(g - j * nch);
-                const int sl = (int)(g % R);
-                const int b = (int)(j % TR);
-                mbar_wait_bounded(&folded[sl], (uint32_t)((g / R) & 1), aborted, a.status);
-                if (c == 0 && j >= TR)  // the store warps have released row j - TR's buffer
-                    mbar_wait_bounded(&tfree[b], (uint32_t)(((j - TR) / TR) & 1), aborted, a.status);
-                tmem_fence_after();
-                if (aborted) break;
-                const int nblk = (std::min(chunk, len - c * chunk) + 1023) / 1024;
-                const uint32_t col = (uint32_t)(b * cpr + c * (chunk / 1024) * 8);
-                const float* slot = ring + (size_t)sl * chunk;
-                for (int k = 0; k < nblk; ++k) tmem_cp_block(tbase + col + 8u * k, slot + 1024 * k);
-                tmem_commit(&freed[sl]);
-                if (c == nch - 1) tmem_commit(&tready[b]);
-                copied = g + 1;
-            }
-            *copied_s = copied;
-        }
-    } else if (warp == kMergeWarp) {
-        // ---------------- merge warp: the group's pairs of each row into its lse
-        for (int64_t j = 0; j < nrows; ++j) {
-            mbar_wait_bounded(&pub[j % kTmemLseRing], (uint32_t)((j / kTmemLseRing) & 1), aborted, a.status);
-            MS mine = ms_empty();
-            for (uint32_t k = (uint32_t)lane; k < GS; k += 32) {
-                const unsigned long long* p = slots + (j % kWsSlots) * GS + k;
-                const MS other = ms_unpack(poll_slot(p, (uint32_t)(j / kWsSlots) & 1u, ld_relaxed_gpu_u64(p),
-                                                     aborted, a.status));
-                mine = ms_merge(mine, other);
-            }
-            const float lv = ms_lse(ms_warp_allreduce(mine));
-            if (lane == 0) {
-                lse_s[j % kTmemLseRing] = lv;
-                mbar_arrive(&lse_full[j % kTmemLseRing]);
-            }
-        }
-    } else {
-        // ---------------- load warp: chunk g + R into slot g % R once chunk g is in tensor memory
-        if (lane == 0) {
-            for (int64_t g = 0; g < std::min<int64_t>(R, total); ++g) issue(g);
-            for (int64_t g = 0; g < total && !aborted; ++g) {
-                if (!mbar_wait_bounded(&freed[g % R], (uint32_t)((g / R) & 1), aborted, a.status)) break;
-                if (g + R < total) issue(g + R);
-            }
-        }
+    using S = MS;
+    using R = float;
+    struct Cursor {
+        float lse;
+        bool softmax;
+    };
+    __device__ static S empty() { return ms_empty(); }
+    template <int K>
+    __device__ static void fold(S& st, const float (&v)[K]) {
+        ms_fold<K>(st, v);
     }
-    __syncthreads();
-    if (warp == kLoadWarp && lane == 0 && atomicAdd(a.status, 0) != 0) {
-        // After a timeout anywhere: one more bounded wait for every bulk copy and the
-        // last tensor-memory copy still in flight before shared and tensor memory are
-        // released (a commit completes after every earlier copy of its thread).
-        bool again = false;
-        for (int64_t g = std::max<int64_t>(0, issued - R); g < issued; ++g)
-            mbar_wait_bounded(&full[g % R], (uint32_t)((g / R) & 1), again, a.status);
-        const long long copied = *copied_s;
-        again = false;
-        if (copied > 0) mbar_wait_bounded(&freed[(copied - 1) % R], (uint32_t)(((copied - 1) / R) & 1), again, a.status);
-    }
-    tmem_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tmem_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols) : "memory");
-    }
-}
-
-__host__ inline size_t smem_tmem_bytes(int chunk, int ring) {
-    return (size_t)ring * chunk * 4 + (size_t)(3 * kRingMax + 2 * kTmemMaxRows + 2 * kTmemLseRing) * 8 + 8 +
-           (kTmemLseRing + 2) * 4 + 64 * sizeof(MS);
-}
+    __device__ static S warp_allreduce(S st) { return ms_warp_allreduce(st); }
+    __device__ static S merge(S x, S y) { return ms_merge(x, y); }
+    __device__ static unsigned long long pack(S st, uint32_t tag) { return ms_pack_tagged(st, tag); }
+    __device__ static S unpack(unsigned long long w, int64_t) { return ms_unpack(w); }
+    __device__ static R finish(S st, const Params&) { return ms_lse(st); }
+    __device__ static Cursor cursor(R lse, const Params& p, int64_t) { return Cursor{lse, p.softmax != 0}; }
+    __device__ static float4 out4(Cursor& c, float4 x, int64_t) { return row_out4(x, c.lse, c.softmax); }
+};
 
 __host__ inline size_t smem_ring_bytes(int chunk, int ring) {
     return (size_t)ring * chunk * 4 + (size_t)kRingMax * 8 + 16 + 64 * sizeof(MS);
@@ -1525,92 +1259,18 @@ cudaError_t launch_lsm_ring_group(const DeviceInfo& dev, const float* x, float* 
     return cudaGetLastError();
 }
 
-// ---- rows parked in tensor memory
-
-// Group size GS (LSE_WS_GROUP forces it), landing chunks of at most LSE_TMEM_CHUNK floats
-// (default 8192; equal chunks, each a multiple of 1024), as many shared-memory slots as
-// fit, and as many tensor-memory row buffers as 512 columns hold (8 columns per 1024
-// floats of the slice, at most kTmemMaxRows, at least 2).  Where the CTAs loop over
-// rows, slices shorter than kTmemMinSlice floats are taken only when no group size
-// gives a longer one: there each row's round trip through the group (publish, merge,
-// store, release) costs more than its bytes, measured on GB300.  Every CTA allocates all of tensor memory,
-// so the plan asks for more than half the SM's shared memory: one CTA per SM, and no
-// CTA of the cooperative grid waits for another's allocation.
+// ---- rows parked in tensor memory (row_tmem.cuh): LSE_WS_GROUP forces the group size,
+// LSE_TMEM_CHUNK (default 8192) bounds the landing chunks.
 cudaError_t plan_lsm_tmem_group(const DeviceInfo& dev, const float* x, const float* out, int64_t rows,
                                 int64_t cols, GroupPlan* plan) {
-    if (cols % 4 != 0 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
-        return cudaErrorNotSupported;
-    const int forced = env_int("LSE_WS_GROUP", 0);
-    const int chunk_env = std::max(1024, env_int("LSE_TMEM_CHUNK", 8192) / 1024 * 1024);
-    const size_t budget = (size_t)dev.max_smem_optin;
-    double best = -1.0;
-    for (int pass = 0; pass < 2 && best < 0; ++pass) {  // pass 0: slices of kTmemMinSlice floats or more
-        for (int GS = 1; GS <= kWsMaxGroup; ++GS) {
-            if (forced && GS != forced) continue;
-            const int64_t sl = ((cols + GS - 1) / GS + 31) / 32 * 32;
-            if (sl * (GS - 1) >= cols || sl > 64 * 1024) continue;
-            if (pass == 0 && !forced && sl < kTmemMinSlice && rows > dev.sm_count / GS) continue;
-            const int cpr = (int)((sl + 1023) / 1024) * 8;
-            const int TR = std::min(kTmemMaxRows, kTmemCols / cpr);
-            if (TR < 2) continue;
-            // equal chunks of at most chunk_env floats, each a whole number of 1024-float blocks
-            const int64_t nch0 = (sl + chunk_env - 1) / chunk_env;
-            const int chunk = (int)(((sl + nch0 - 1) / nch0 + 1023) / 1024 * 1024);
-            const int nch = (int)((sl + chunk - 1) / chunk);
-            const int R = (int)std::min<int64_t>(kRingMax, (int64_t)(budget - smem_tmem_bytes(0, 0)) / ((int64_t)chunk * 4));
-            if (R < 2) continue;
-            const size_t smem = std::max(smem_tmem_bytes(chunk, R), budget / 2 + 1024);  // one CTA per SM
-            if (smem > budget) continue;
-            const int64_t groups = std::min<int64_t>(rows, dev.sm_count / GS);
-            if (groups < 1) continue;
-            const double score = (double)(groups * GS) / dev.sm_count - 0.002 * GS +
-                                 0.01 * std::min(8.0, TR + (double)R / nch);
-            if (score > best) {
-                best = score;
-                plan->threads = 32 * (8 + 4 + 3);
-                plan->nbuf = R * 100 + TR;  // landing slots and tensor-memory row buffers
-                plan->group_size = GS;
-                plan->groups = (int)groups;
-                plan->slice = (int)sl;
-                plan->chunk = chunk;
-                plan->smem = smem;
-                plan->scratch_bytes = (size_t)groups * kWsSlots * GS * sizeof(unsigned long long);
-            }
-        }
-    }
-    return best < 0 ? cudaErrorNotSupported : cudaSuccess;
+    return plan_row_tmem(dev, x, out, rows, cols, env_int("LSE_WS_GROUP", 0), env_int("LSE_TMEM_CHUNK", 8192), 16384,
+                         plan);
 }
 
 cudaError_t launch_lsm_tmem_group(const DeviceInfo& dev, const float* x, float* out, int64_t rows, int64_t cols,
                                   const GroupPlan& p, void* scratch, cudaStream_t stream, bool softmax) {
-    cudaError_t e = cudaMemsetAsync(scratch, 0xFF, p.scratch_bytes, stream);
-    if (e != cudaSuccess) return e;
-    const int R = p.nbuf / 100, TR = p.nbuf % 100;
-    if (env_int("LSE_VERBOSE", 0))
-        fprintf(stderr, "[lse] lsm_tmem group: GS=%d groups=%d slots=%d tmem_rows=%d slice=%d chunk=%d smem=%zu\n",
-                p.group_size, p.groups, R, TR, p.slice, p.chunk, p.smem);
-    SmemRowArgs args{x, out, rows, cols, p.slice, p.chunk, dev.status, p.group_size,
-                     static_cast<unsigned long long*>(scratch), softmax ? 1 : 0, R, TR};
-    auto kern = lsm_tmem_kernel<8, 4>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, p.threads, p.smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm != 1) return cudaErrorNotSupported;  // each CTA holds all of the SM's tensor memory
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the group waits end
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.blockDim = dim3((unsigned)p.threads);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = stream;
-    cfg.gridDim = dim3((unsigned)(p.groups * p.group_size));
-    e = cudaLaunchKernelEx(&cfg, kern, args);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_row_tmem<LsmOp, 4>(dev, x, out, rows, cols, p, scratch, stream, LsmOp::Params{softmax ? 1 : 0},
+                                     "row_tmem (log_softmax)");
 }
 
 // ------------------------------------------------------------------ rows re-read from L2 by a group

@@ -268,11 +268,14 @@ lse_status_t check_rows(const float* x, const float* out, int64_t rows, int64_t 
 // The one-kernel GroupNorm chain with output kind out_kind (0 channel lse,
 // 1 GroupNorm, 2 chain before the lse), scratch from the device pool.
 // By default the channel lse takes the work queue with per-thread loads and the
-// elementwise outputs the bulk-copy work queue.  LSE_GN_VARIANT 2 forces the
+// elementwise outputs the (sample, group) slabs as rows of the tensor-memory row kernel
+// (the bulk-copy work queue where that does not apply).  LSE_GN_VARIANT 2 forces the
 // work-queue kernel with per-thread loads, 3 the one with bulk-copy staging, 4 the
 // sample-slice kernel (y read once, slices kept in shared memory; the channel lse
 // only, where it applies; measured slower on GB300), 5 the tile queue with tiles
-// parked in tensor memory (y read once; the channel lse only, where it applies).
+// parked in tensor memory (y read once; the channel lse only, where it applies), 6 the
+// (sample, group) slabs as rows of the tensor-memory row kernel (GroupNorm and the
+// chain before the lse, where it applies).
 lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, float* out, int64_t N, int64_t C,
                       int64_t HW, int64_t G, float eps, int out_kind, cudaStream_t stream) {
     DeviceState* s = nullptr;
@@ -281,6 +284,20 @@ lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, flo
     cudaMemPool_t pool = nullptr;
     if ((st = device_pool(s, &pool)) != LSE_OK) return st;
     const int variant = env_int("LSE_GN_VARIANT", 0);
+    if (out_kind != 0 && (variant == 6 || variant == 0)) {
+        // the slabs as rows parked in tensor memory: y read once, out written once
+        GroupPlan plan;
+        if (plan_gn_rows(s->info, y, out, N, C, HW, G, out_kind, &plan) == cudaSuccess) {
+            void* scratch = nullptr;
+            cudaError_t e = pool_alloc(&scratch, plan.scratch_bytes, pool, stream);
+            if (e != cudaSuccess) return cuda_fail(e);
+            e = launch_gn_rows(s->info, y, gamma, beta, out, N, C, HW, G, eps, plan, scratch, stream, out_kind);
+            cudaError_t ef = cudaFreeAsync(scratch, stream);
+            if (e == cudaSuccess && ef == cudaSuccess) return LSE_OK;
+            if (e != cudaErrorNotSupported) return cuda_fail(e != cudaSuccess ? e : ef);
+            (void)cudaGetLastError();  // not launchable here: the default path below
+        }
+    }
     if (out_kind == 0 && variant == 5) {
         // the channel lse with y read once: tiles parked in tensor memory
         GnTmemPlan plan;

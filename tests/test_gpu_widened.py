@@ -213,9 +213,13 @@ def _gn(L, fn, inp, G, eps=1e-5, misalign=False):
     return out.cpu()
 
 
+@pytest.mark.parametrize("variant", ["0", "3"])
 @pytest.mark.parametrize("fn", ["group_norm", "gn_act_residual"])
 @pytest.mark.parametrize("N,C,H,W,G", GN_CASES)
-def test_gn_elementwise_parity(lib, fn, N, C, H, W, G):
+def test_gn_elementwise_parity(lib, env, fn, N, C, H, W, G, variant):
+    """The default (slab rows in tensor memory where HW % 4 == 0 and the pointers are
+    16-byte aligned, else the bulk-copy work queue) and the bulk-copy work queue itself."""
+    env.setenv("LSE_GN_VARIANT", variant)
     inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))
     got = _gn(lib, fn, inp, G)
     ref = getattr(oracle, fn)(inp["y"], inp["gamma"], inp["beta"], G, 1e-5)
@@ -253,9 +257,10 @@ def test_gn_elementwise_non_finite(lib, env, fn, variant):
 @pytest.mark.parametrize("cfg", [{"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "5", "LSE_GN_LAG": "0"},
                                  {"LSE_GN_VARIANT": "2", "LSE_GN_PARTS": "16", "LSE_GN_LAG": "100",
                                   "LSE_GN_CTAS_PER_SM": "1"},
-                                 {"LSE_GNT_SLOTS": "1", "LSE_GNT_LAG": "0"},
-                                 {"LSE_GNT_SLOTS": "2", "LSE_GNT_LAG": "3", "LSE_GNT_CTAS_PER_SM": "1"},
-                                 {"LSE_GNT_SLOTS": "6", "LSE_GNT_LAG": "100"}],
+                                 {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "1", "LSE_GNT_LAG": "0"},
+                                 {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "2", "LSE_GNT_LAG": "3",
+                                  "LSE_GNT_CTAS_PER_SM": "1"},
+                                 {"LSE_GN_VARIANT": "3", "LSE_GNT_SLOTS": "6", "LSE_GNT_LAG": "100"}],
                          ids=["queue-p5", "queue-p16", "tma-s1", "tma-s2", "tma-s6"])
 @pytest.mark.parametrize("fn", ["group_norm", "gn_act_residual"])
 def test_gn_elementwise_configs(lib, env, cfg, fn):
@@ -267,7 +272,71 @@ def test_gn_elementwise_configs(lib, env, cfg, fn):
                   f"{fn} {cfg}")
 
 
-def test_group_norm_wide_range(lib):
+GN_ROW_CASES = [
+    (5, 64, 20, 20, 16),     # slabs of 1,600 floats: one CTA or a few per slab
+    (3, 64, 126, 126, 16),   # the full image: slabs of 63,504 floats over several CTAs
+    (7, 32, 40, 40, 8),      # ragged last slice
+    (2, 8, 64, 64, 2),       # slabs of 16,384 floats
+    (40, 16, 32, 32, 4),     # 160 slabs: more rows than SMs
+    (300, 4, 16, 16, 1),     # 300 one-group samples: the CTAs loop over rows
+    (2, 6, 4, 4, 3),         # two channels per group, 32-float slabs
+]
+
+
+@pytest.mark.parametrize("cfg", [{}, {"LSE_GNR_GROUP": "2"}, {"LSE_GNR_GROUP": "19"},
+                                 {"LSE_GNR_GROUP": "3", "LSE_GNR_CHUNK": "1024"}],
+                         ids=["plan", "gs2", "gs19", "gs3-chunk1k"])
+@pytest.mark.parametrize("fn", ["group_norm", "gn_act_residual"])
+@pytest.mark.parametrize("N,C,H,W,G", GN_ROW_CASES)
+def test_gn_rows_parity(lib, env, fn, N, C, H, W, G, cfg):
+    """The (sample, group) slabs as rows parked in tensor memory (LSE_GN_VARIANT=6)."""
+    env.setenv("LSE_GN_VARIANT", "6")
+    for k, v in cfg.items():
+        env.setenv(k, v)
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))
+    got = _gn(lib, fn, inp, G)
+    ref = getattr(oracle, fn)(inp["y"], inp["gamma"], inp["beta"], G, 1e-5)
+    assert_parity(got, ref, f"{fn} rows {N,C,H,W,G} {cfg}")
+
+
+@pytest.mark.parametrize("fn", ["group_norm", "gn_act_residual"])
+def test_gn_rows_non_finite(lib, env, fn):
+    """test_gn_elementwise_non_finite with 48 pixels (HW % 4 == 0: the row kernel takes it)."""
+    env.setenv("LSE_GN_VARIANT", "6")
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(4, 16, 6, 8))
+    y = inp["y"].clone()
+    y[0, 5, 2, 3] = float("nan")
+    y[1, 1, 0, 0] = float("inf")
+    y[2, 10, 5, 6] = float("-inf")
+    inp["y"] = y
+    got = _gn(lib, fn, inp, 4)
+    nan = torch.isnan(got)
+    assert int(nan.sum()) == 3 * 4 * 48
+    assert bool(nan[0, 4:8].all() and nan[1, 0:4].all() and nan[2, 8:12].all())
+    assert_parity(got, getattr(oracle, fn)(y, inp["gamma"], inp["beta"], 4, 1e-5), f"{fn} rows non-finite y")
+
+
+@pytest.mark.parametrize("variant", ["0", "6"])
+def test_group_norm_large_mean(lib, env, variant):
+    """Mean 100 times the spread (1e2 and 0.5): the mean is subtracted before scaling and the
+    variance is not E[y^2] - E[y]^2 (which in fp32 would be off by ~1e-3 relative here).
+    The regime stays where an fp32 GroupNorm can meet the tolerance: z inherits the mean's
+    half-ulp times rstd * gamma (8e-6 here; 3e-4 at mean 1e3 and spread 0.1, the chain's
+    own large-mean test, where the output's magnitude widens the tolerance)."""
+    env.setenv("LSE_GN_VARIANT", variant)
+    N, C, H, W, G = 2, 16, 40, 40, 4
+    inp = {"y": synth.normal((N, C, H, W), seed=81, mean=1.0e2, var=0.25),
+           "gamma": synth.uniform((C,), seed=82, lo=0.5, hi=1.5),
+           "beta": synth.normal((C,), seed=83, var=0.1)}
+    for fn in ("group_norm", "gn_act_residual"):
+        got = _gn(lib, fn, inp, G)
+        assert_parity(got, getattr(oracle, fn)(inp["y"], inp["gamma"], inp["beta"], G, 1e-5),
+                      f"{fn} mean 1e3 v{variant}")
+
+
+@pytest.mark.parametrize("variant", ["0", "6"])
+def test_group_norm_wide_range(lib, env, variant):
+    env.setenv("LSE_GN_VARIANT", variant)
     N, C, H, W, G = 2, 16, 20, 20, 4
     inp = {"y": synth.normal((N, C, H, W), seed=77, mean=30.0, var=25.0),
            "gamma": synth.uniform((C,), seed=78, lo=-3.0, hi=3.0),
