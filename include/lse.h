@@ -58,8 +58,10 @@
  *     slices held in shared memory by groups of CTAs, y read once (gn_act_lse
  *     only, HW % 4 == 0, C <= 256, G <= 64; falls back otherwise), 5 a queue
  *     of 256-pixel tiles parked in tensor memory, y read once (gn_act_lse
- *     only, HW % 4 == 0, C % 4 == 0, C <= 64; falls back otherwise); default 2
- *     for gn_act_lse, 3 for group_norm and gn_act_residual),
+ *     only, HW % 4 == 0, C % 4 == 0, C <= 64; falls back otherwise), 6 the
+ *     (sample, group) slabs as rows parked in tensor memory (group_norm and
+ *     gn_act_residual, HW % 4 == 0 and 16-byte aligned y and out); default 2
+ *     for gn_act_lse, 6 (else 3) for group_norm and gn_act_residual),
  *     LSE_CONV_CHAIN (conv_gn_act_lse: 1 y and its tiles' statistics from
  *     the convolution's epilogue, then merge and apply; 2 y never in memory;
  *     3 y, then the GroupNorm work queue over it; default 3), LSE_CONV_TMA
@@ -76,8 +78,10 @@
  *     LSE_GN_CTAS_PER_SM and LSE_GNT_SLOTS / LSE_GNT_LAG / LSE_GNT_CTAS_PER_SM
  *     (the two GroupNorm work queues), LSE_SLAB_GROUP / LSE_SLAB_NB (CTAs per
  *     sample and slice buffers of the sample-slice kernel), LSE_GNM_SLOTS
- *     (landing slots of the tensor-memory tile queue), LSE_HOST_CHUNK_MB (host
- *     pipeline chunk).
+ *     (landing slots of the tensor-memory tile queue), LSE_GNR_GROUP /
+ *     LSE_GNR_CHUNK / LSE_GNR_SW (CTAs per slab, floats per landing chunk,
+ *     store warps 4 or 8 of the slab rows), LSE_HOST_CHUNK_MB (host pipeline
+ *     chunk).
  *   - LSE_VERBOSE=1 prints each launch's plan on stderr.
  *   - Test hooks, not for production: LSE_TEST_FAIL_ALLOC=1 makes every
  *     scratch allocation fail (the call returns LSE_ERR_CUDA and enqueues
@@ -191,9 +195,12 @@ lse_status_t log_softmax_dim(const float* x, float* out, int64_t outer, int64_t 
  *   gamma  [C], beta [C] fp32, device, read only.
  *   out    [N * C * HW] fp32, device, written (must not alias y).
  *   N >= 0, HW >= 0, 1 <= C <= 8192, G >= 1, C % G == 0; eps >= 0 and finite.
- * One cooperative kernel: the statistics of a sample, then its normalised
- * output written from a second read of the sample served by L2.  Scratch and
- * error rules as gn_act_lse.
+ * One cooperative kernel.  Where HW % 4 == 0 and y and out are 16-byte
+ * aligned, each (sample, group) slab (C/G x HW contiguous floats) is a row
+ * split over a few CTAs: read once into tensor memory, its mean and M2 merged
+ * across the CTAs, then written normalised; otherwise a work queue computes a
+ * sample's statistics, then its output from a second read served by L2.
+ * Scratch and error rules as gn_act_lse.
  */
 lse_status_t group_norm(const float* y, const float* gamma, const float* beta, float* out,
                         int64_t N, int64_t C, int64_t HW, int64_t G, float eps,

@@ -10,7 +10,8 @@
 //  rows_reg_kernel      rows up to 32K floats: the row lives in registers of
 //                       one warp or one block; exact two-pass (max, then sum)
 //                       over registers, one HBM read and one write.
-//  lsm_tmem_kernel      (the default for long 16-byte-aligned rows) a row split
+//  row_tmem_kernel      (row_tmem.cuh, with LsmOp below; the default for long
+//                       16-byte-aligned rows) a row split
 //                       over a group of CTAs of a cooperative grid; each slice
 //                       lands chunk by chunk in shared memory (bulk copies),
 //                       is folded there and copied on into tensor memory
