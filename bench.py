@@ -941,11 +941,13 @@ def run_ours(args, w: synth.Workload):
     return 0
 
 
-def host_link(host_in, dev, max_bytes=1 << 30, min_bytes=64 << 20):
+def host_link(host_in, dev, host_out=None, max_bytes=1 << 30, min_bytes=64 << 20):
     """Copy-engine bandwidth of this process's host link on its own pinned input buffer
     (after the end-to-end timing, which no longer needs it): host to device from its
     first half, device to host into its second half, and both at once (two streams),
-    GB/s.  None when the buffer is too small to time bandwidth rather than latency."""
+    GB/s; and device to host into the output buffer the end-to-end steps wrote
+    (`d2h_out_gbs`: pinned buffers can differ in how fast the copy engines reach them).
+    None when the buffer is too small to time bandwidth rather than latency."""
     buf = max(host_in.values(), key=lambda t: t.numel()).view(-1)
     n = int(min(buf.numel() // 2, max_bytes // 4))
     if n * 4 < min_bytes:
@@ -977,7 +979,12 @@ def host_link(host_in, dev, max_bytes=1 << 30, min_bytes=64 << 20):
     h2d = n * 4 / min(timed(lambda: a.copy_(src, non_blocking=True)) for _ in range(2)) / 1e9
     d2h = n * 4 / min(timed(lambda: dst.copy_(a, non_blocking=True)) for _ in range(2)) / 1e9
     bi = 2 * n * 4 / min(timed(both) for _ in range(2)) / 1e9
-    return {"h2d_gbs": round(h2d, 1), "d2h_gbs": round(d2h, 1), "both_gbs": round(bi, 1), "bytes_each": n * 4}
+    res = {"h2d_gbs": round(h2d, 1), "d2h_gbs": round(d2h, 1), "both_gbs": round(bi, 1), "bytes_each": n * 4}
+    if host_out is not None and host_out.numel() >= n:
+        dout = host_out.view(-1)[:n]
+        dout.copy_(a, non_blocking=True)
+        res["d2h_out_gbs"] = round(n * 4 / min(timed(lambda: dout.copy_(a, non_blocking=True)) for _ in range(2)) / 1e9, 1)
+    return res
 
 
 def e2e_ceiling(nbytes, h2d_bytes, d2h_bytes, link):
@@ -1034,7 +1041,7 @@ def run_e2e(L, w: synth.Workload, inputs, args, dev, world):
            "d2h_bytes_per_step": d2h, "steps": steps,
            "note": "pinned host buffers; every step copies its input in and its result out "
                    "(log_softmax: chunked pipeline overlapping both copies with the call)"}
-    link = host_link(host_in, dev)
+    link = host_link(host_in, dev, host_out)
     if link is not None:
         ceil = e2e_ceiling(nbytes, h2d, d2h, link)
         out["host_link"] = link
