@@ -292,6 +292,228 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
     if (warp == 0) tmem_dealloc(tmem_slot, alloc_cols);
 }
 
+// conv2d_ws_kernel: the y-writing convolution (Cout <= 64, products stacked) as a
+// pipeline of warp roles, so that the tensor cores, the hi / lo split and the y stores
+// of different tiles overlap instead of running in series per tile slot:
+//   load warp     bulk-copies tile i's raw window into raw[i % 4] once the split of
+//                 tile i - 4 has released it;
+//   split warps   two warpgroups, alternate tiles: raw[i % 4] into the hi / lo window
+//                 win[i % 4] (once tile i - 4's MMAs are done with it);
+//   MMA warps     two, alternate tiles: tile i's 18 MMAs from win[i % 4] into accumulator
+//                 i % 4 of tensor memory (once tile i - 4's epilogue has read it),
+//                 committed to the window's and the accumulator's barriers;
+//   epilogue      four warpgroups, tiles in turn: the accumulator's two halves plus
+//                 the bias, written to y (lane m of the accumulator is wide pixel m).
+// Each ring is indexed by the CTA's tile number and every role's members divide the ring,
+// so each entry has one member per role, and no barrier completes twice before its
+// waiter has seen the first phase.
+// Waits are bounded.
+constexpr int kCwRing = 4;     // raw windows, split windows and accumulators in flight
+constexpr int kCwMma = 2;      // MMA warps (alternate tiles; kCwRing a multiple)
+constexpr int kCwSplitWG = 2;  // split warpgroups
+constexpr int kCwEpiWG = 4;    // epilogue warpgroups
+constexpr int kCwSplit0 = 1 + kCwMma, kCwEpi0 = kCwSplit0 + 4 * kCwSplitWG;  // first warp of each
+constexpr int kCwThreads = 32 * (kCwEpi0 + 4 * kCwEpiWG);
+// Ring ownership: tile i goes to member i mod (members) of each role, and the members
+// divide the ring, so one member waits on each entry's barriers, in phase order.  A
+// waiter that came to phase k + 1 of a barrier still in phase k would read the parity
+// of phase k - 1 as its own; a timed-out run with three epilogue warpgroups (not a
+// divisor of four) did exactly that.
+static_assert(kCwRing % kCwMma == 0 && kCwRing % kCwSplitWG == 0 && kCwRing % kCwEpiWG == 0, "ring ownership");
+
+__host__ __device__ static inline size_t conv_ws_smem(int cout, int S) {
+    return conv_weight_bytes(cout) + (size_t)kCwRing * (conv_raw_bytes(S) + (size_t)S * 16 * 2 * 2);
+}
+
+template <int CIN>
+__global__ void __launch_bounds__(kCwThreads, 1) conv2d_ws_kernel(const ConvArgs a) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ uint64_t raw_full[kCwRing], raw_free[kCwRing], win_full[kCwRing], win_free[kCwRing];
+    __shared__ uint64_t acc_full[kCwRing], acc_free[kCwRing];
+    __shared__ uint32_t tmem_slot;
+    __shared__ long long mma_done_s[kCwMma];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = a.S, W = a.W, cout = a.cout;
+    unsigned char* const bw = smem_raw;  // the nine B operands, hi and lo rows
+    float* const bias = reinterpret_cast<float*>(bw + (size_t)cout * 9 * 8 * 4 * 2);
+    const size_t raw_bytes = conv_raw_bytes(S), win_bytes = (size_t)S * 16 * 2 * 2;
+    unsigned char* const rawbase = smem_raw + conv_weight_bytes(cout);
+    unsigned char* const winbase = rawbase + kCwRing * raw_bytes;
+    auto rawp = [&](int r) { return reinterpret_cast<float*>(rawbase + (size_t)r * raw_bytes); };
+    auto whi = [&](int w) { return winbase + (size_t)w * win_bytes; };
+    auto wlo = [&](int w) { return winbase + (size_t)w * win_bytes + (size_t)S * 16 * 2; };
+    const uint32_t ncols = conv_tmem_cols(cout);  // 2 Cout (stacked), at most 128
+
+    if (warp == 0) tmem_alloc(&tmem_slot, 512);
+    if (tid == 0) {
+        for (int k = 0; k < kCwRing; ++k) {
+            mbar_init(&raw_full[k], 1);
+            mbar_init(&raw_free[k], kConvTileM);
+            mbar_init(&win_full[k], kConvTileM);
+            mbar_init(&win_free[k], 1);
+            mbar_init(&acc_full[k], 1);
+            mbar_init(&acc_free[k], 4);
+        }
+        for (int m = 0; m < kCwMma; ++m) mma_done_s[m] = 0;
+        fence_mbar_init();
+    }
+    conv_stage_weights(a.w, a.cin, cout, bw);
+    for (int c = tid; c < cout; c += blockDim.x) bias[c] = a.b[c];
+    fence_proxy_async_smem();  // the weights are read by the tensor cores (async proxy)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const int64_t plane = (int64_t)a.H * W;
+    const int64_t ohw = (int64_t)a.OH * a.OW;
+    const int64_t total = a.N * a.tiles;
+    const int64_t nit = (int64_t)blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    auto tile_of = [&](int64_t i) { return (int64_t)blockIdx.x + i * gridDim.x; };
+    bool aborted = false;
+    int64_t issued = 0;  // load warp: raw windows requested
+
+    if (warp == 0) {
+        // ---------------- load warp
+        if (lane == 0) {
+            for (int64_t i = 0; i < nit; ++i) {
+                const int r = (int)(i % kCwRing);
+                if (i >= kCwRing) mbar_wait_bounded(&raw_free[r], (uint32_t)((i / kCwRing - 1) & 1), aborted, a.status);
+                if (aborted) break;
+                const int64_t t = tile_of(i), n = t / a.tiles;
+                conv_fetch_window<CIN>(a.x + n * a.cin * plane, plane, (t - n * a.tiles) * kConvTileM, S, rawp(r),
+                                       &raw_full[r]);
+                issued = i + 1;
+            }
+        }
+    } else if (warp <= kCwMma) {
+        // ---------------- MMA warps, alternate tiles: the whole warp runs the loop and its
+        // waits (uniform branches), lane 0 issues.  The tensor pipe's queue is short: an
+        // issuing warp's control between tiles (waits, fences, the lane-0 region) measured
+        // 300 to 600 clocks per tile of idle pipe on GB300 with one issuing warp, and
+        // about a tenth of that with two, each filling the other's gaps.
+        const int mw = warp - 1;
+        ConvStackedMma mm;
+        mm.init(bw, W, S, cout);
+        long long done = 0;  // 1 + the last tile this warp issued
+        for (int64_t i = mw; i < nit; i += kCwMma) {
+            const int w = (int)(i % kCwRing);
+            mbar_wait_bounded(&win_full[w], (uint32_t)((i / kCwRing) & 1), aborted, a.status);
+            if (i >= kCwRing) mbar_wait_bounded(&acc_free[w], (uint32_t)((i / kCwRing - 1) & 1), aborted, a.status);
+            if (__any_sync(0xffffffffu, aborted)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                mm.issue(tmem + (uint32_t)w * ncols, whi(w), wlo(w));
+                umma_commit(&win_free[w]);
+                umma_commit(&acc_full[w]);  // the same MMAs
+            }
+            __syncwarp();
+            done = i + 1;
+        }
+        if (lane == 0) mma_done_s[mw] = done;
+    } else if (warp < kCwEpi0) {
+        // ---------------- split warpgroups: raw[i % 4] -> win[i % 4], alternate tiles
+        const int sg = (warp - kCwSplit0) / 4, st = tid - 32 * kCwSplit0 - sg * kConvTileM;
+        for (int64_t i = sg; i < nit; i += kCwSplitWG) {
+            const int r = (int)(i % kCwRing);
+            mbar_wait_bounded(&raw_full[r], (uint32_t)((i / kCwRing) & 1), aborted, a.status);
+            if (i >= kCwRing) mbar_wait_bounded(&win_free[r], (uint32_t)((i / kCwRing - 1) & 1), aborted, a.status);
+            const int64_t t = tile_of(i), n = t / a.tiles;
+            conv_split_window<CIN, true>(rawp(r), plane, (t - n * a.tiles) * kConvTileM, S, st, kConvTileM, whi(r),
+                                         wlo(r));
+            fence_proxy_async_smem();  // the window is read by the tensor cores
+            mbar_arrive(&raw_free[r]);
+            mbar_arrive(&win_full[r]);
+        }
+    } else {
+        // ---------------- epilogue warpgroups: accumulator i % 4 -> y, alternate tiles
+        const int eg = (warp - kCwEpi0) / 4;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int m = 32 * (warp & 3) + lane;  // accumulator lane of this thread: wide pixel q0 + m
+        for (int64_t i = eg; i < nit; i += kCwEpiWG) {
+            const int ac = (int)(i % kCwRing);
+            mbar_wait_bounded(&acc_full[ac], (uint32_t)((i / kCwRing) & 1), aborted, a.status);
+            tc_fence_after();
+            __syncwarp();
+            const int64_t t = tile_of(i), n = t / a.tiles;
+            const int64_t q = (t - n * a.tiles) * kConvTileM + m;
+            const int64_t oh = q / W;
+            const int ow = (int)(q - oh * W);
+            const bool valid = ow < a.OW && oh < a.OH;
+            float* dst = a.y + n * cout * ohw + oh * a.OW + ow;
+            const uint32_t d = tmem + (uint32_t)ac * ncols + lane_base;
+            for (int c0 = 0; c0 < cout; c0 += 16) {
+                float v[16], vl[16];  // A_hi [B_hi; B_lo] halves, and A_lo B_hi added into the first
+                tmem_ld16(d + (uint32_t)c0, v);
+                tmem_ld16(d + (uint32_t)(cout + c0), vl);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += vl[j];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += bias[c0 + j];
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dst[(int64_t)(c0 + j) * ohw] = v[j];
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_free[ac]);
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && atomicAdd(a.status, 0) != 0) {
+        // After a timeout anywhere: one more bounded wait for the raw windows and the MMAs
+        // still in flight before shared and tensor memory are released (a commit
+        // completes after every earlier MMA of its thread).
+        bool again = false;
+        for (int64_t i = std::max<int64_t>(0, issued - kCwRing); i < issued; ++i)
+            mbar_wait_bounded(&raw_full[i % kCwRing], (uint32_t)((i / kCwRing) & 1), again, a.status);
+        for (int m = 0; m < kCwMma; ++m) {  // a commit tracks its own thread's MMAs
+            const long long done = mma_done_s[m];
+            again = false;
+            if (done > 0)
+                mbar_wait_bounded(&acc_full[(done - 1) % kCwRing], (uint32_t)(((done - 1) / kCwRing) & 1), again,
+                                  a.status);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// The pipelined kernel where it applies: y written, Cout <= 64 in multiples of 16 (the
+// stacked products), raw windows by bulk copies (16-byte aligned planes), its rings in
+// shared memory.  cudaErrorNotSupported otherwise (LSE_CONV_WS=0 forces that too).
+// Its rings take 96 S bytes per entry (S = conv_window(W)): up to W = 187 at Cout = 64.
+template <int CIN>
+static cudaError_t conv_ws_go(const DeviceInfo& dev, const ConvArgs& a0, cudaStream_t stream) {
+    ConvArgs a = a0;
+    if (env_int("LSE_CONV_WS", 1) == 0 || !conv_stacked(a.cout) || a.cout % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(a.x) & 15) != 0 || ((int64_t)a.H * a.W) % 4 != 0 || env_int("LSE_CONV_TMA", 1) == 0)
+        return cudaErrorNotSupported;
+    const size_t need = conv_ws_smem(a.cout, a.S), budget = (size_t)dev.max_smem_optin - 1024;
+    if (need > budget) return cudaErrorNotSupported;
+    // more than half the shared memory: one CTA per SM (each allocates all of tensor memory)
+    const size_t smem = std::max(need, std::min(budget, (size_t)dev.max_smem_optin / 2 + 1024));
+    auto kern = conv2d_ws_kernel<CIN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCwThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm != 1) return cudaErrorNotSupported;  // each CTA allocates all of tensor memory
+    a.tma = 1;
+    const int64_t total = a.N * a.tiles;
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(total, dev.sm_count));
+    if (env_int("LSE_VERBOSE", 0))
+        fprintf(stderr, "[lse] conv2d_ws: grid=%u window=%d tiles=%lld smem=%zu\n", grid, a.S, (long long)total, smem);
+    kern<<<grid, kCwThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
 bool conv_tc_supported(int64_t cin, int64_t cout, int64_t W) {
     return cin >= 1 && cin <= kConvMaxCin && cout >= 16 && cout <= 128 && cout % 16 == 0 && W <= kConvMaxW;
 }
@@ -299,16 +521,23 @@ bool conv_tc_supported(int64_t cin, int64_t cout, int64_t W) {
 template <int CIN, int CPG, int MODE>
 static cudaError_t conv_go(const DeviceInfo& dev, const ConvArgs& a, cudaStream_t stream);
 
+template <int CIN>
+static cudaError_t conv_write_y(const DeviceInfo& dev, const ConvArgs& a, cudaStream_t stream) {
+    cudaError_t e = conv_ws_go<CIN>(dev, a, stream);
+    if (e != cudaErrorNotSupported) return e;
+    return conv_go<CIN, 0, kConvWriteY>(dev, a, stream);
+}
+
 static cudaError_t conv_dispatch(const DeviceInfo& dev, const ConvArgs& a, cudaStream_t stream) {
     switch (a.cin) {
-        case 1: return conv_go<1, 0, kConvWriteY>(dev, a, stream);
-        case 2: return conv_go<2, 0, kConvWriteY>(dev, a, stream);
-        case 3: return conv_go<3, 0, kConvWriteY>(dev, a, stream);
-        case 4: return conv_go<4, 0, kConvWriteY>(dev, a, stream);
-        case 5: return conv_go<5, 0, kConvWriteY>(dev, a, stream);
-        case 6: return conv_go<6, 0, kConvWriteY>(dev, a, stream);
-        case 7: return conv_go<7, 0, kConvWriteY>(dev, a, stream);
-        default: return conv_go<8, 0, kConvWriteY>(dev, a, stream);
+        case 1: return conv_write_y<1>(dev, a, stream);
+        case 2: return conv_write_y<2>(dev, a, stream);
+        case 3: return conv_write_y<3>(dev, a, stream);
+        case 4: return conv_write_y<4>(dev, a, stream);
+        case 5: return conv_write_y<5>(dev, a, stream);
+        case 6: return conv_write_y<6>(dev, a, stream);
+        case 7: return conv_write_y<7>(dev, a, stream);
+        default: return conv_write_y<8>(dev, a, stream);
     }
 }
 
@@ -457,7 +686,7 @@ cudaError_t launch_conv_gn_act_lse(const DeviceInfo& dev, const float* x, const 
     if (conv_chain_mode() == 3) {
         // y, then the one-kernel GroupNorm chain over it, samples last to first so
         // that its first statistics reads find the convolution's last samples in L2
-        cudaError_t e = conv_go<8, 0, kConvWriteY>(dev, a, stream);
+        cudaError_t e = conv_write_y<8>(dev, a, stream);
         if (e != cudaSuccess) return e;
         return launch_gn_act_lse_fused(dev, y, gamma, beta, out, N, cout, ohw, G, eps, sp, stream, 0, true);
     }

@@ -195,3 +195,17 @@ def test_conv2d_window_paths(lib, tma, monkeypatch):
     for shape in ((3, 8, 20, 24, 64), (1, 8, 130, 132, 64), (2, 3, 9, 12, 16)):
         inp = _inputs(*shape, seed=3)
         assert_parity(_conv(lib, inp), oracle.conv2d(inp["x"], inp["w"], inp["bias"]), f"conv tma={tma} {shape}")
+
+
+@pytest.mark.parametrize("ws", ["0", "1"], ids=["tile-slots", "pipeline"])
+def test_conv2d_pipeline_paths(lib, ws, monkeypatch):
+    """The pipelined kernel (warp roles, rings of four raw windows, split windows and
+    accumulators) and the tile-slot kernel: several tiles per CTA so that every ring
+    wraps, fewer tiles than SMs, every stacked Cout, a ragged last tile, the widest rows
+    its rings take; Cout = 128 (not stacked) and planes of H W % 4 != 0 (no bulk copies)
+    take the tile-slot kernel either way."""
+    monkeypatch.setenv("LSE_CONV_WS", ws)
+    for shape in ((12, 8, 128, 128, 64), (1, 8, 20, 24, 64), (4, 8, 32, 47, 16), (3, 5, 40, 36, 32),
+                  (2, 8, 60, 70, 48), (1, 8, 130, 131, 128), (2, 8, 50, 180, 64), (2, 8, 61, 70, 48)):
+        inp = _inputs(*shape, seed=5)
+        assert_parity(_conv(lib, inp), oracle.conv2d(inp["x"], inp["w"], inp["bias"]), f"conv ws={ws} {shape}")
