@@ -98,7 +98,7 @@ LAUNCHES = {
     "log_softmax_dim0": ["lse_strided_kernel"],
     "group_norm": ["row_tmem_kernel"],
     "gn_act_residual": ["row_tmem_kernel"],
-    "conv_gn_act_lse": ["conv2d_tc_kernel", "gn_fused_kernel"],
+    "conv_gn_act_lse": ["conv2d_ws_kernel", "gn_fused_kernel"],
 }
 
 
@@ -265,7 +265,7 @@ KERNEL_SOURCES = {
     "lse_strided_kernel": ["lse_strided.cu"],
     "gn_fused_kernel": ["gn_act_lse.cu", "gn_common.cuh"],
     "gn_tma_kernel": ["gn_tma.cu", "gn_common.cuh"],
-    "conv2d_tc_kernel": ["conv.cu", "conv_tile.cuh", "gn_common.cuh"],
+    "conv2d_ws_kernel": ["conv.cu", "conv_tile.cuh", "gn_common.cuh"],
 }
 
 
@@ -775,7 +775,7 @@ def measure_config(L, name: str, role: str, kind: str, dev, stream, steps: int, 
                 conv()
             per_c, _, t0c, t1c = time_steps(conv, steps, flush, stream, dev)
             ms_c = statistics.mean(per_c)
-            res["conv2d_3x3"] = {"kernel": "conv2d_tc_kernel", "ms_per_call": round(ms_c, 5),
+            res["conv2d_3x3"] = {"kernel": "conv2d_ws_kernel", "ms_per_call": round(ms_c, 5),
                                  "tflops_method": round(fl / (ms_c / 1e3) / 1e12, 2),
                                  "frac_of_tf32_peak": round(fl / (ms_c / 1e3) / 1e12 / tpk, 4)}
             windows.append((t0c, t1c))
