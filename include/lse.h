@@ -60,8 +60,12 @@
  *     of 256-pixel tiles parked in tensor memory, y read once (gn_act_lse
  *     only, HW % 4 == 0, C % 4 == 0, C <= 64; falls back otherwise), 6 the
  *     (sample, group) slabs as rows parked in tensor memory (group_norm and
- *     gn_act_residual, HW % 4 == 0 and 16-byte aligned y and out); default 2
- *     for gn_act_lse, 6 (else 3) for group_norm and gn_act_residual),
+ *     gn_act_residual, HW % 4 == 0 and 16-byte aligned y and out), 7 the
+ *     whole grid on one sample at a time, each CTA a pixel slice of all
+ *     channels in shared memory, y read once (gn_act_lse only, HW % 4 == 0
+ *     with slices of at most 256 pixels, C % 4 == 0, C <= 64, G <= 64; falls
+ *     back otherwise); default 2 for gn_act_lse, 6 (else 3) for group_norm
+ *     and gn_act_residual),
  *     LSE_CONV_CHAIN (conv_gn_act_lse: 1 y and its tiles' statistics from
  *     the convolution's epilogue, then merge and apply; 2 y never in memory;
  *     3 y, then the GroupNorm work queue over it; default 3), LSE_CONV_TMA
@@ -78,7 +82,9 @@
  *     LSE_GN_CTAS_PER_SM and LSE_GNT_SLOTS / LSE_GNT_LAG / LSE_GNT_CTAS_PER_SM
  *     (the two GroupNorm work queues), LSE_SLAB_GROUP / LSE_SLAB_NB (CTAs per
  *     sample and slice buffers of the sample-slice kernel), LSE_GNM_SLOTS
- *     (landing slots of the tensor-memory tile queue), LSE_GNR_GROUP /
+ *     (landing slots of the tensor-memory tile queue), LSE_GNS_SLOTS (slots
+ *     of the whole-grid sweep, 3 or more), LSE_CONV_WS (0: the convolution's
+ *     tile-slot kernel instead of the pipelined one), LSE_GNR_GROUP /
  *     LSE_GNR_CHUNK / LSE_GNR_SW (CTAs per slab, floats per landing chunk,
  *     store warps 4 or 8 of the slab rows), LSE_HOST_CHUNK_MB (host pipeline
  *     chunk).

@@ -154,6 +154,22 @@ cudaError_t launch_gn_tmem(const DeviceInfo& dev, const float* y, const float* g
                            int64_t N, int64_t C, int64_t HW, int64_t G, float eps, const GnTmemPlan& plan,
                            void* scratch, cudaStream_t stream);
 
+// Form 3 with y read once, the whole grid on one sample at a time: CTA j holds pixel
+// slice j of all C channels of each sample in a ring of shared-memory slots, the group
+// statistics are grid-wide fp64 sums (the channel lse only).  gn_sweep_plan says whether
+// it applies (HW % 4 == 0 with a slice of at most 256 pixels, 4 <= C <= 64 with
+// C % 4 == 0, G <= 64, 16-byte aligned y, at least three slots) and sizes the launch and
+// its scratch.
+struct GnSweepPlan {
+    int grid = 0, PB = 0, R = 0, threads = 0;
+    size_t smem = 0, scratch_bytes = 0;
+};
+bool gn_sweep_plan(const DeviceInfo& dev, const float* y, int64_t N, int64_t C, int64_t HW, int64_t G,
+                   GnSweepPlan* plan);
+cudaError_t launch_gn_sweep(const DeviceInfo& dev, const float* y, const float* gamma, const float* beta, float* out,
+                            int64_t N, int64_t C, int64_t HW, int64_t G, float eps, const GnSweepPlan& plan,
+                            void* scratch, cudaStream_t stream);
+
 // Form 3 with y read once: each sample split by pixels over a group of CTAs that
 // keep their slices in shared memory and exchange per-group partial statistics
 // through global slots (the channel lse only).  gn_slab_plan says whether it

@@ -275,7 +275,8 @@ lse_status_t check_rows(const float* x, const float* out, int64_t rows, int64_t 
 // only, where it applies; measured slower on GB300), 5 the tile queue with tiles
 // parked in tensor memory (y read once; the channel lse only, where it applies), 6 the
 // (sample, group) slabs as rows of the tensor-memory row kernel (GroupNorm and the
-// chain before the lse, where it applies).
+// chain before the lse, where it applies), 7 the whole grid on one sample at a time
+// (y read once; the channel lse only, where it applies).
 lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, float* out, int64_t N, int64_t C,
                       int64_t HW, int64_t G, float eps, int out_kind, cudaStream_t stream) {
     DeviceState* s = nullptr;
@@ -292,6 +293,20 @@ lse_status_t gn_fused(const float* y, const float* gamma, const float* beta, flo
             cudaError_t e = pool_alloc(&scratch, plan.scratch_bytes, pool, stream);
             if (e != cudaSuccess) return cuda_fail(e);
             e = launch_gn_rows(s->info, y, gamma, beta, out, N, C, HW, G, eps, plan, scratch, stream, out_kind);
+            cudaError_t ef = cudaFreeAsync(scratch, stream);
+            if (e == cudaSuccess && ef == cudaSuccess) return LSE_OK;
+            if (e != cudaErrorNotSupported) return cuda_fail(e != cudaSuccess ? e : ef);
+            (void)cudaGetLastError();  // not launchable here: the default path below
+        }
+    }
+    if (out_kind == 0 && variant == 7) {
+        // the channel lse with y read once: the whole grid on one sample at a time
+        GnSweepPlan plan;
+        if (gn_sweep_plan(s->info, y, N, C, HW, G, &plan)) {
+            void* scratch = nullptr;
+            cudaError_t e = pool_alloc(&scratch, plan.scratch_bytes, pool, stream);
+            if (e != cudaSuccess) return cuda_fail(e);
+            e = launch_gn_sweep(s->info, y, gamma, beta, out, N, C, HW, G, eps, plan, scratch, stream);
             cudaError_t ef = cudaFreeAsync(scratch, stream);
             if (e == cudaSuccess && ef == cudaSuccess) return LSE_OK;
             if (e != cudaErrorNotSupported) return cuda_fail(e != cudaSuccess ? e : ef);

@@ -73,7 +73,7 @@ def test_strided_ops(lib, shift):
 
 @pytest.mark.parametrize("shift", [0, 1])
 def test_groupnorm_ops(lib, shift, monkeypatch):
-    for variant in ("0", "1", "2", "3", "4", "5", "6"):
+    for variant in ("0", "1", "2", "3", "4", "5", "6", "7"):
         monkeypatch.setenv("LSE_GN_VARIANT", variant)
         for N, C, H, W, G in ((3, 64, 12, 12, 16), (2, 8, 5, 7, 4), (5, 16, 8, 8, 4)):
             inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))

@@ -86,7 +86,7 @@ def test_log_softmax_4096x393216(lib):
     del x, out
 
 
-@pytest.mark.parametrize("variant", ["0", "5"])
+@pytest.mark.parametrize("variant", ["0", "5", "7"])
 def test_gn_act_lse_128x64x126x126(lib, monkeypatch, variant):
     monkeypatch.setenv("LSE_GN_VARIANT", variant)
     inp = synth.make_inputs("gn_act_lse_128x64x126x126", device=DEV)

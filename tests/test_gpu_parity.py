@@ -303,6 +303,8 @@ GN_CONFIGS = [
     {"LSE_GN_VARIANT": "4", "LSE_SLAB_GROUP": "2"},
     {"LSE_GN_VARIANT": "5"},                                    # tiles parked in tensor memory
     {"LSE_GN_VARIANT": "5", "LSE_GNM_SLOTS": "2"},
+    {"LSE_GN_VARIANT": "7"},                                    # the whole grid on one sample at a time
+    {"LSE_GN_VARIANT": "7", "LSE_GNS_SLOTS": "3"},
 ]
 
 
@@ -329,7 +331,7 @@ def _non_finite_gn_input():
     return y, inp["gamma"], inp["beta"]
 
 
-@pytest.mark.parametrize("variant", ["0", "1", "2", "3", "4"])
+@pytest.mark.parametrize("variant", ["0", "1", "2", "3", "4", "7"])
 def test_gn_act_lse_non_finite(lib, env, variant):
     """A non-finite value makes its group's mean or variance NaN, so every channel of that
     group is NaN at every pixel and the sample's channel lse is NaN everywhere; the
@@ -358,6 +360,30 @@ def test_gn_tmem_shapes(lib, env, N, C, H, W, G):
     got = lib.gn_act_lse_forward(inp["y"].to(DEV), inp["gamma"].to(DEV), inp["beta"].to(DEV), G, 1e-5)
     ref = oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], G, 1e-5)
     assert_parity(got, ref, f"gn tmem {N,C,H,W,G}")
+
+
+@pytest.mark.parametrize("N,C,H,W,G,slots", [
+    (3, 64, 33, 40, 16, 0),     # slices of 8 and 12 pixels
+    (2, 12, 16, 16, 3, 0),      # 6 channels per apply half: pairs only, no batch of 8
+    (1, 4, 2, 2, 1, 0),         # one quad: a grid of one CTA
+    (2, 32, 32, 32, 8, 0),
+    (7, 64, 20, 20, 4, 0),      # 16 channels per group
+    (2, 64, 12, 12, 64, 0),     # one channel per group, 64 groups: both table lanes
+    (2, 60, 10, 10, 15, 0),     # 15 groups of 4
+    (6, 64, 126, 126, 16, 0),   # the full image: slices of 104 and 108 pixels
+    (3, 64, 160, 152, 16, 0),   # slices of 160 pixels: two apply blocks (128 + 32)
+    (50, 8, 16, 16, 2, 3),      # three slots: the ring wraps 16 times
+])
+def test_gn_sweep_shapes(lib, env, N, C, H, W, G, slots):
+    """The whole grid on one sample at a time (slices of every channel in shared memory,
+    grid-wide fp64 sums) on ragged and extreme shapes."""
+    env.setenv("LSE_GN_VARIANT", "7")
+    if slots:
+        env.setenv("LSE_GNS_SLOTS", str(slots))
+    inp = synth.make_inputs("gn_act_lse_128x64x126x126", shape=(N, C, H, W))
+    got = lib.gn_act_lse_forward(inp["y"].to(DEV), inp["gamma"].to(DEV), inp["beta"].to(DEV), G, 1e-5)
+    ref = oracle.gn_act_lse(inp["y"], inp["gamma"], inp["beta"], G, 1e-5)
+    assert_parity(got, ref, f"gn sweep {N,C,H,W,G}")
 
 
 def test_gn_tmem_non_finite(lib, env):
@@ -394,7 +420,7 @@ def test_gn_max_channels(lib, env, variant, N, H, W, G):
                       f"{fn} C=8192 G={G} v{variant}")
 
 
-@pytest.mark.parametrize("variant", ["0", "5"])
+@pytest.mark.parametrize("variant", ["0", "5", "7"])
 def test_gn_act_lse_wide_range(lib, env, variant):
     """Large gamma and shifted data: z spans about [-60, 60] (tanh saturates),
     a non-zero mean exercises the statistics."""
@@ -407,7 +433,7 @@ def test_gn_act_lse_wide_range(lib, env, variant):
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-3), "gn wide")
 
 
-@pytest.mark.parametrize("variant", ["0", "5"])
+@pytest.mark.parametrize("variant", ["0", "5", "7"])
 def test_gn_act_lse_large_mean_small_spread(lib, env, variant):
     """Groups whose mean (1e3) is 1e4 times their spread (std 0.1, so rstd ~ 10): z stays
     accurate (the mean is subtracted before scaling, and the tile-queue kernel merges its
@@ -424,7 +450,7 @@ def test_gn_act_lse_large_mean_small_spread(lib, env, variant):
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-5), "gn mean 1e3, std 0.1")
 
 
-@pytest.mark.parametrize("variant", ["0", "5"])
+@pytest.mark.parametrize("variant", ["0", "5", "7"])
 @pytest.mark.parametrize("scale", [1.0e3, 1.0e6, 1.0e15])
 def test_gn_act_lse_large_values(lib, env, scale, variant):
     """y of magnitude up to 1e15 with channels far apart: the running max and its
@@ -438,7 +464,7 @@ def test_gn_act_lse_large_values(lib, env, scale, variant):
     assert_parity(got, oracle.gn_act_lse(y, gamma, beta, G, 1e-5), f"gn scale {scale}")
 
 
-@pytest.mark.parametrize("variant", ["0", "5"])
+@pytest.mark.parametrize("variant", ["0", "5", "7"])
 def test_gn_act_lse_constant_group(lib, env, variant):
     """Zero variance in a group: z = beta exactly (eps keeps rstd finite).  20 x 20
     pixels: two tiles, whose merged M2 stays exactly 0."""
