@@ -292,14 +292,14 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
     if (warp == 0) tmem_dealloc(tmem_slot, alloc_cols);
 }
 
-// conv2d_ws_kernel: the y-writing convolution (Cout <= 64, products stacked) as a
-// pipeline of warp roles, so that the tensor cores, the hi / lo split and the y stores
+// conv2d_ws_kernel: the y-writing convolution (Cout <= 96) as a pipeline of warp roles, so that the tensor cores, the hi / lo split and the y stores
 // of different tiles overlap instead of running in series per tile slot:
 //   load warp     bulk-copies tile i's raw window into raw[i % 4] once the split of
 //                 tile i - 4 has released it;
 //   split warps   two warpgroups, alternate tiles: raw[i % 4] into the hi / lo window
 //                 win[i % 4] (once tile i - 4's MMAs are done with it);
-//   MMA warps     two, alternate tiles: tile i's 18 MMAs from win[i % 4] into accumulator
+//   MMA warps     two, alternate tiles: tile i's 18 MMAs (27 at Cout 80 and 96, products
+//                 not stacked) from win[i % 4] into accumulator
 //                 i % 4 of tensor memory (once tile i - 4's epilogue has read it),
 //                 committed to the window's and the accumulator's barriers;
 //   epilogue      four warpgroups, tiles in turn: the accumulator's two halves plus
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kCwThreads, 1) conv2d_ws_kernel(const ConvArgs
         // 300 to 600 clocks per tile of idle pipe on GB300 with one issuing warp, and
         // about a tenth of that with two, each filling the other's gaps.
         const int mw = warp - 1;
-        ConvStackedMma mm;
+        ConvTileMma mm;
         mm.init(bw, W, S, cout);
         long long done = 0;  // 1 + the last tile this warp issued
         for (int64_t i = mw; i < nit; i += kCwMma) {
@@ -444,13 +444,19 @@ __global__ void __launch_bounds__(kCwThreads, 1) conv2d_ws_kernel(const ConvArgs
             const bool valid = ow < a.OW && oh < a.OH;
             float* dst = a.y + n * cout * ohw + oh * a.OW + ow;
             const uint32_t d = tmem + (uint32_t)ac * ncols + lane_base;
+            const bool stacked = conv_stacked(cout);
             for (int c0 = 0; c0 < cout; c0 += 16) {
-                float v[16], vl[16];  // A_hi [B_hi; B_lo] halves, and A_lo B_hi added into the first
+                float v[16];
                 tmem_ld16(d + (uint32_t)c0, v);
-                tmem_ld16(d + (uint32_t)(cout + c0), vl);
-                tmem_wait_ld();
+                if (stacked) {
+                    float vl[16];  // stacked: the A_hi B_lo half, added into the first
+                    tmem_ld16(d + (uint32_t)(cout + c0), vl);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] += vl[j];
+                    for (int j = 0; j < 16; ++j) v[j] += vl[j];
+                } else {
+                    tmem_wait_ld();
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] += bias[c0 + j];
                 if (valid) {
@@ -484,14 +490,17 @@ __global__ void __launch_bounds__(kCwThreads, 1) conv2d_ws_kernel(const ConvArgs
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// The pipelined kernel where it applies: y written, Cout <= 64 in multiples of 16 (the
-// stacked products), raw windows by bulk copies (16-byte aligned planes), its rings in
-// shared memory.  cudaErrorNotSupported otherwise (LSE_CONV_WS=0 forces that too).
-// Its rings take 96 S bytes per entry (S = conv_window(W)): up to W = 187 at Cout = 64.
+// The pipelined kernel where it applies: y written, Cout <= 96 in multiples of 16, raw
+// windows by bulk copies (16-byte aligned planes), its rings in shared memory;
+// cudaErrorNotSupported otherwise (LSE_CONV_WS=0 forces that too).  Its rings take 96 S
+// bytes per entry (S = conv_window(W)) beside the weights: up to W = 187 at Cout = 64.
+// Measured on GB300 at x[128, 8, 128, 128] against the tile-slot kernel: Cout 64
+// 0.129 / 0.168 ms, 96 0.212 / 0.225, but 128 0.313 / 0.279 (27 MMAs and 64 KB of y
+// stores per tile: the tile slots overlap them better), so wider layers keep the slots.
 template <int CIN>
 static cudaError_t conv_ws_go(const DeviceInfo& dev, const ConvArgs& a0, cudaStream_t stream) {
     ConvArgs a = a0;
-    if (env_int("LSE_CONV_WS", 1) == 0 || !conv_stacked(a.cout) || a.cout % 16 != 0 ||
+    if (env_int("LSE_CONV_WS", 1) == 0 || a.cout > 96 || a.cout % 16 != 0 ||
         (reinterpret_cast<uintptr_t>(a.x) & 15) != 0 || ((int64_t)a.H * a.W) % 4 != 0 || env_int("LSE_CONV_TMA", 1) == 0)
         return cudaErrorNotSupported;
     const size_t need = conv_ws_smem(a.cout, a.S), budget = (size_t)dev.max_smem_optin - 1024;

@@ -232,16 +232,17 @@ __device__ __forceinline__ void conv_issue_mma(uint32_t d_tmem, const unsigned c
     umma_commit(bar);
 }
 
-// The stacked tile MMAs (Cout <= 64) with every descriptor but the window's built
-// once: the nine B descriptors and the taps' window offsets stay in the issuing
-// thread's registers, so a tile is 18 MMAs with one add each.  An issue loop that
-// rebuilds descriptors per MMA (several integer operations each, the tap's
-// division by three) measured 1.5x to 3.5x slower on GB300 than the tensor pipe
-// (56 clocks per MMA at M = 128, N = 128 / 64, K = 8).
-struct ConvStackedMma {
+// The tile MMAs with every descriptor but the window's built once: the nine B
+// descriptors and the taps' window offsets stay in the issuing thread's registers, so a
+// tile is 18 (stacked, Cout <= 64) or 27 MMAs with one add each.  An issue loop that
+// rebuilds descriptors per MMA (several integer operations each, the tap's division by
+// three) measured 1.5x to 3.5x slower on GB300 than the tensor pipe (56 clocks per MMA at
+// M = 128, N = 128 / 64, K = 8).
+struct ConvTileMma {
     uint64_t b[9];   // tap t: [B_hi; B_lo] (N = 2 Cout; its first Cout rows are B_hi)
     uint32_t oa[9];  // tap t's window offset, 16-byte units: (t / 3) W + t % 3
-    uint32_t idesc, idesc2, lbo_a;
+    uint32_t idesc, idesc2, lbo_a, lo16;
+    bool stacked;
 
     __device__ __forceinline__ void init(const unsigned char* b_smem, int W, int S, int cout) {
         const uint32_t lbo_b = conv_lbo_b(cout), sb = smem_u32(b_smem);
@@ -253,15 +254,27 @@ struct ConvStackedMma {
         idesc = umma_idesc_tf32(kConvTileM, cout);
         idesc2 = umma_idesc_tf32(kConvTileM, 2 * cout);
         lbo_a = (uint32_t)S * 16;
+        lo16 = (uint32_t)(cout / 8) * 128 / 16;  // B_lo's rows: the start field moved by Cout / 8 core matrices
+        stacked = conv_stacked(cout);
     }
-    // A_hi [B_hi; B_lo] and A_lo B_hi of the nine taps into D at d_tmem (the window's
-    // start field plus an offset: shared addresses stay below 2^18, no carry out of it).
+    // Stacked: A_hi [B_hi; B_lo] and A_lo B_hi of the nine taps into D at d_tmem; else
+    // A_hi B_hi, A_hi B_lo and A_lo B_hi, all N = Cout (the windows' start fields plus an
+    // offset: shared addresses stay below 2^18, no carry out of the field).
     __device__ __forceinline__ void issue(uint32_t d_tmem, const unsigned char* ahi, const unsigned char* alo) const {
         const uint64_t dh = umma_desc(smem_u32(ahi), lbo_a, 128), dl = umma_desc(smem_u32(alo), lbo_a, 128);
+        if (stacked) {
 #pragma unroll
-        for (int t = 0; t < 9; ++t) {
-            umma_tf32(d_tmem, dh + oa[t], b[t], idesc2, t > 0);
-            umma_tf32(d_tmem, dl + oa[t], b[t], idesc, 1);
+            for (int t = 0; t < 9; ++t) {
+                umma_tf32(d_tmem, dh + oa[t], b[t], idesc2, t > 0);
+                umma_tf32(d_tmem, dl + oa[t], b[t], idesc, 1);
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 9; ++t) {
+                umma_tf32(d_tmem, dh + oa[t], b[t], idesc, t > 0);
+                umma_tf32(d_tmem, dh + oa[t], b[t] + lo16, idesc, 1);
+                umma_tf32(d_tmem, dl + oa[t], b[t], idesc, 1);
+            }
         }
     }
 };

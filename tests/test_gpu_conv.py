@@ -201,11 +201,13 @@ def test_conv2d_window_paths(lib, tma, monkeypatch):
 def test_conv2d_pipeline_paths(lib, ws, monkeypatch):
     """The pipelined kernel (warp roles, rings of four raw windows, split windows and
     accumulators) and the tile-slot kernel: several tiles per CTA so that every ring
-    wraps, fewer tiles than SMs, every stacked Cout, a ragged last tile, the widest rows
-    its rings take; Cout = 128 (not stacked) and planes of H W % 4 != 0 (no bulk copies)
-    take the tile-slot kernel either way."""
+    wraps, fewer tiles than SMs, every stacked Cout, unstacked Cout 96 (three products per
+    tap), a ragged last tile, the widest rows its rings take; Cout 112 and 128 and planes
+    of H W % 4 != 0 (no bulk copies) take the tile-slot kernel either way."""
     monkeypatch.setenv("LSE_CONV_WS", ws)
     for shape in ((12, 8, 128, 128, 64), (1, 8, 20, 24, 64), (4, 8, 32, 47, 16), (3, 5, 40, 36, 32),
-                  (2, 8, 60, 70, 48), (1, 8, 130, 131, 128), (2, 8, 50, 180, 64), (2, 8, 61, 70, 48)):
+                  (2, 8, 60, 70, 48), (1, 8, 130, 131, 128), (2, 8, 50, 180, 64), (2, 8, 61, 70, 48),
+                  (4, 8, 64, 64, 128), (3, 8, 20, 36, 96), (1, 8, 128, 128, 112), (2, 8, 30, 132, 128),
+                  (2, 8, 12, 140, 128)):
         inp = _inputs(*shape, seed=5)
         assert_parity(_conv(lib, inp), oracle.conv2d(inp["x"], inp["w"], inp["bias"]), f"conv ws={ws} {shape}")
