@@ -292,18 +292,20 @@ __global__ void __launch_bounds__(kConvMaxSlots * kConvTileM, 1) conv2d_tc_kerne
     if (warp == 0) tmem_dealloc(tmem_slot, alloc_cols);
 }
 
-// conv2d_ws_kernel: the y-writing convolution (Cout <= 96) as a pipeline of warp roles, so that the tensor cores, the hi / lo split and the y stores
-// of different tiles overlap instead of running in series per tile slot:
+// conv2d_ws_kernel: the y-writing convolution (Cout <= 96) as a pipeline of warp roles, so
+// that the tensor cores, the hi / lo split and the y stores of different tiles overlap
+// instead of running in series per tile slot:
 //   load warp     bulk-copies tile i's raw window into raw[i % 4] once the split of
 //                 tile i - 4 has released it;
 //   split warps   two warpgroups, alternate tiles: raw[i % 4] into the hi / lo window
 //                 win[i % 4] (once tile i - 4's MMAs are done with it);
 //   MMA warps     two, alternate tiles: tile i's 18 MMAs (27 at Cout 80 and 96, products
-//                 not stacked) from win[i % 4] into accumulator
-//                 i % 4 of tensor memory (once tile i - 4's epilogue has read it),
-//                 committed to the window's and the accumulator's barriers;
-//   epilogue      four warpgroups, tiles in turn: the accumulator's two halves plus
-//                 the bias, written to y (lane m of the accumulator is wide pixel m).
+//                 not stacked) from win[i % 4] into accumulator i % 4 of tensor memory
+//                 (once tile i - 4's epilogue has read it), committed to the window's and
+//                 the accumulator's barriers;
+//   epilogue      four warpgroups, tiles in turn: the accumulator (its two halves added
+//                 where the products are stacked) plus the bias, written to y (lane m of
+//                 the accumulator is wide pixel m).
 // Each ring is indexed by the CTA's tile number and every role's members divide the ring,
 // so each entry has one member per role, and no barrier completes twice before its
 // waiter has seen the first phase.
