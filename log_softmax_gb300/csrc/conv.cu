@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kCwThreads, 1) conv2d_ws_kernel(const ConvArgs
     auto rawp = [&](int r) { return reinterpret_cast<float*>(rawbase + (size_t)r * raw_bytes); };
     auto whi = [&](int w) { return winbase + (size_t)w * win_bytes; };
     auto wlo = [&](int w) { return winbase + (size_t)w * win_bytes + (size_t)S * 16 * 2; };
-    const uint32_t ncols = conv_tmem_cols(cout);  // 2 Cout (stacked), at most 128
+    const uint32_t ncols = conv_tmem_cols(cout);  // accumulator columns: 2 Cout (stacked) or Cout, at most 128
 
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
     if (tid == 0) {
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kCwThreads, 1) conv2d_ws_kernel(const ConvArgs
             mbar_arrive(&win_full[r]);
         }
     } else {
-        // ---------------- epilogue warpgroups: accumulator i % 4 -> y, alternate tiles
+        // ---------------- epilogue warpgroups: accumulator i % 4 -> y, tiles in turn
         const int eg = (warp - kCwEpi0) / 4;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int m = 32 * (warp & 3) + lane;  // accumulator lane of this thread: wide pixel q0 + m
