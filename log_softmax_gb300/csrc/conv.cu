@@ -432,6 +432,7 @@ __global__ void __launch_bounds__(kCwThreads, 1) conv2d_ws_kernel(const ConvArgs
     } else {
         // ---------------- epilogue warpgroups: accumulator i % 4 -> y, tiles in turn
         const int eg = (warp - kCwEpi0) / 4;
+        const uint64_t drop = l2_policy_evict_first();
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const int m = 32 * (warp & 3) + lane;  // accumulator lane of this thread: wide pixel q0 + m
         for (int64_t i = eg; i < nit; i += kCwEpiWG) {
@@ -462,8 +463,13 @@ __global__ void __launch_bounds__(kCwThreads, 1) conv2d_ws_kernel(const ConvArgs
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] += bias[c0 + j];
                 if (valid) {
+                    // y is written once: evict-first lines (on GB300 2-3 % faster than plain
+                    // stores on one box, equal on another; the chain that reads y back unchanged)
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) dst[(int64_t)(c0 + j) * ohw] = v[j];
+                    for (int j = 0; j < 16; ++j)
+                        asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst + (int64_t)(c0 + j) * ohw),
+                                     "f"(v[j]), "l"(drop)
+                                     : "memory");
                 }
             }
             tc_fence_before();
